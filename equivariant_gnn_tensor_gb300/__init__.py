@@ -1,0 +1,275 @@
+"""Python binding of libtpconv.so, the sm_103a fused equivariant
+tensor-product convolution (see include/tpconv.h for the C contract).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels. PyTorch supplies device memory and the current CUDA
+stream. Importing this package raises if the library has not been built;
+there is no CPU fallback.
+
+Entry points (same names as the C ABI)::
+
+    desc = tp_desc_create("128x0e+128x1o+128x2e", "0e+1o+2e+3o", "128x0e+128x1o+128x2e")
+    sh = tp_spherical_harmonics(desc, vec)                 # [E, dim_sh]
+    perm, row_ptr, dst_sorted = tp_csr_build(dst, n_dst)   # stable, dst-sorted CSR
+    out = tp_conv_forward(desc, x, sh, w, src, row_ptr, n_dst)
+    dx, dw, dsh = tp_conv_backward(desc, grad_out, x, sh, w, src, dst_sorted, row_ptr,
+                                   src_perm, src_row_ptr)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtpconv.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+                      " (or python equivariant_gnn_tensor_gb300/build.py)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+TP_OK = 0
+STATUS_NAMES = {0: "TP_OK", 1: "TP_ERR_PARSE", 2: "TP_ERR_UNSUPPORTED", 3: "TP_ERR_UNSORTED", 4: "TP_ERR_INDEX",
+                5: "TP_ERR_ALIGN", 6: "TP_ERR_CUDA", 7: "TP_ERR_ARG", 8: "TP_ERR_TIMEOUT"}
+TP_F32, TP_BF16_IN_F32_OUT = 0, 1
+TP_IR_MUL, TP_MUL_IR = 0, 1
+TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
+EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
+           "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_conv_forward",
+           "tp_conv_backward", "tp_device_status", "tp_status_string", "tp_abi_version"]
+
+
+class TPError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _lib.tp_status_string(status).decode()
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({msg})")
+
+
+class _Info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "n_paths", "mul", "dim_x", "dim_sh", "dim_out", "weight_numel", "n_in", "n_sh", "n_out",
+        "lmax_in", "lmax_sh", "lmax_out", "cg_nnz")]
+
+
+class _Path(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("a", "b", "c", "la", "lb", "lc")]
+
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_sigs = {
+    "tp_desc_create": [ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(_vp)],
+    "tp_desc_query": [_vp, ctypes.POINTER(_Info)],
+    "tp_desc_path": [_vp, _i32, ctypes.POINTER(_Path)],
+    "tp_desc_cg": [_vp, _i32, _vp, _i64],
+    "tp_spherical_harmonics": [_vp, _vp, _i64, _i32, _vp, _vp],
+    "tp_csr_workspace_size": [_i64, _i32, ctypes.POINTER(_sz)],
+    "tp_csr_build": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _sz, _vp],
+    "tp_conv_forward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp],
+    "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
+    "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
+}
+for _n, _a in _sigs.items():
+    getattr(_lib, _n).argtypes = _a
+    getattr(_lib, _n).restype = ctypes.c_int
+_lib.tp_desc_destroy.argtypes = [_vp]
+_lib.tp_desc_destroy.restype = None
+_lib.tp_status_string.argtypes = [ctypes.c_int]
+_lib.tp_status_string.restype = ctypes.c_char_p
+_lib.tp_abi_version.argtypes = []
+_lib.tp_abi_version.restype = ctypes.c_int32
+
+
+def _check(status: int, what: str):
+    if status != TP_OK:
+        raise TPError(status, what)
+
+
+class Descriptor:
+    """Owns a tp_desc (host memory); fields mirror tp_desc_info."""
+
+    def __init__(self, handle: int, irreps):
+        self._h = _vp(handle)
+        self.irreps_in, self.irreps_sh, self.irreps_out = irreps
+        info = _Info()
+        _check(_lib.tp_desc_query(self._h, ctypes.byref(info)), "tp_desc_query")
+        for f, _ in _Info._fields_:
+            setattr(self, f, int(getattr(info, f)))
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            _lib.tp_desc_destroy(h)
+            self._h = _vp(0)
+
+    def __repr__(self):
+        return (f"Descriptor({self.irreps_in!r} x {self.irreps_sh!r} -> {self.irreps_out!r}, "
+                f"paths={self.n_paths}, weight_numel={self.weight_numel})")
+
+
+def tp_abi_version() -> int:
+    return int(_lib.tp_abi_version())
+
+
+def tp_status_string(status: int) -> str:
+    return _lib.tp_status_string(status).decode()
+
+
+def tp_desc_create(irreps_in: str, irreps_sh: str, irreps_out: str, layout: str = "ir_mul") -> Descriptor:
+    lay = {"ir_mul": TP_IR_MUL, "mul_ir": TP_MUL_IR}[layout]
+    h = _vp()
+    _check(_lib.tp_desc_create(irreps_in.encode(), irreps_sh.encode(), irreps_out.encode(), lay, ctypes.byref(h)),
+           "tp_desc_create")
+    return Descriptor(h.value, (irreps_in, irreps_sh, irreps_out))
+
+
+def tp_desc_query(desc: Descriptor) -> dict:
+    return {f: getattr(desc, f) for f, _ in _Info._fields_}
+
+
+def tp_desc_path(desc: Descriptor, p: int) -> tuple:
+    info = _Path()
+    _check(_lib.tp_desc_path(desc.handle, p, ctypes.byref(info)), "tp_desc_path")
+    return (info.a, info.b, info.c, info.la, info.lb, info.lc)
+
+
+def tp_desc_cg(desc: Descriptor, p: int) -> np.ndarray:
+    a, b, c, la, lb, lc = tp_desc_path(desc, p)
+    out = np.zeros((2 * la + 1, 2 * lb + 1, 2 * lc + 1), dtype=np.float64)
+    _check(_lib.tp_desc_cg(desc.handle, p, out.ctypes.data_as(_vp), out.size), "tp_desc_cg")
+    return out
+
+
+# --- tensors -----------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return _vp(t.data_ptr()) if t is not None and t.numel() > 0 else _vp(0)
+
+
+def _dev_ptr(t, name, dtype=None, ndim=None):
+    torch = _torch()
+    if t is None:
+        return _vp(0)
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    return _vp(t.data_ptr()) if t.numel() > 0 else _vp(0)
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return _vp(s.cuda_stream)
+
+
+def tp_spherical_harmonics(desc: Descriptor, vec, normalize: bool = True, out=None, stream=None):
+    """Real harmonics of the desc's harmonic irreps for vec [E, 3] float32."""
+    torch = _torch()
+    E = vec.shape[0]
+    if out is None:
+        out = torch.empty((E, desc.dim_sh), dtype=torch.float32, device=vec.device)
+    _check(_lib.tp_spherical_harmonics(desc.handle, _dev_ptr(vec, "vec", torch.float32, 2), E, int(bool(normalize)),
+                                       _dev_ptr(out, "sh", torch.float32, 2), _stream(stream)),
+           "tp_spherical_harmonics")
+    return out
+
+
+def tp_csr_workspace_size(E: int, N: int) -> int:
+    n = _sz()
+    _check(_lib.tp_csr_workspace_size(E, N, ctypes.byref(n)), "tp_csr_workspace_size")
+    return int(n.value)
+
+
+def tp_csr_build(keys, N: int, perm=None, row_ptr=None, keys_sorted=None, workspace=None, stream=None):
+    """Stable counting sort of int32 keys in [0, N) -> (perm, row_ptr, keys_sorted)."""
+    torch = _torch()
+    E = keys.shape[0]
+    dev = keys.device
+    if perm is None:
+        perm = torch.empty(E, dtype=torch.int32, device=dev)
+    if row_ptr is None:
+        row_ptr = torch.empty(N + 1, dtype=torch.int32, device=dev)
+    if keys_sorted is None:
+        keys_sorted = torch.empty(E, dtype=torch.int32, device=dev)
+    ws_bytes = tp_csr_workspace_size(E, N)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _check(_lib.tp_csr_build(_dev_ptr(keys, "keys", torch.int32, 1), E, N, _dev_ptr(perm, "perm", torch.int32, 1),
+                             _dev_ptr(row_ptr, "row_ptr", torch.int32, 1),
+                             _dev_ptr(keys_sorted, "keys_sorted", torch.int32, 1),
+                             _dev_ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)),
+           "tp_csr_build")
+    return perm, row_ptr, keys_sorted
+
+
+def tp_conv_forward(desc: Descriptor, x, sh, w, src, row_ptr, n_dst: int, out=None, stream=None):
+    """out[n_dst, dim_out] float32 for destination-sorted edges. x and w are both
+    float32 (TP_F32) or both bfloat16 (TP_BF16_IN_F32_OUT)."""
+    torch = _torch()
+    if x.dtype != w.dtype:
+        raise TypeError("x and w must have the same dtype")
+    dtype = {torch.float32: TP_F32, torch.bfloat16: TP_BF16_IN_F32_OUT}.get(x.dtype)
+    if dtype is None:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    E = src.shape[0]
+    if out is None:
+        out = torch.empty((n_dst, desc.dim_out), dtype=torch.float32, device=x.device)
+    _check(_lib.tp_conv_forward(desc.handle, dtype, _dev_ptr(x, "x", None, 2), _dev_ptr(sh, "sh", torch.float32, 2),
+                                _dev_ptr(w, "w", None, 2), _dev_ptr(src, "src", torch.int32, 1),
+                                _dev_ptr(row_ptr, "row_ptr", torch.int32, 1), x.shape[0], n_dst, E,
+                                _dev_ptr(out, "out", torch.float32, 2), _stream(stream)),
+           "tp_conv_forward")
+    return out
+
+
+def tp_conv_backward(desc: Descriptor, grad_out, x, sh, w, src, dst, row_ptr, src_perm, src_row_ptr,
+                     dx=None, dw=None, dsh=None, stream=None):
+    """(dx, dw, dsh) float32 for destination-sorted edges; (src_perm,
+    src_row_ptr) is tp_csr_build(src, n_src) in that edge order."""
+    torch = _torch()
+    E = src.shape[0]
+    n_src, n_dst = x.shape[0], grad_out.shape[0]
+    if dx is None:
+        dx = torch.empty((n_src, desc.dim_x), dtype=torch.float32, device=x.device)
+    if dw is None:
+        dw = torch.empty((E, desc.weight_numel), dtype=torch.float32, device=x.device)
+    if dsh is None:
+        dsh = torch.empty((E, desc.dim_sh), dtype=torch.float32, device=x.device)
+    f = torch.float32
+    _check(_lib.tp_conv_backward(desc.handle, _dev_ptr(grad_out, "grad_out", f, 2), _dev_ptr(x, "x", f, 2),
+                                 _dev_ptr(sh, "sh", f, 2), _dev_ptr(w, "w", f, 2),
+                                 _dev_ptr(src, "src", torch.int32, 1), _dev_ptr(dst, "dst", torch.int32, 1),
+                                 _dev_ptr(row_ptr, "row_ptr", torch.int32, 1),
+                                 _dev_ptr(src_perm, "src_perm", torch.int32, 1),
+                                 _dev_ptr(src_row_ptr, "src_row_ptr", torch.int32, 1), n_src, n_dst, E,
+                                 _dev_ptr(dx, "dx", f, 2), _dev_ptr(dw, "dw", f, 2), _dev_ptr(dsh, "dsh", f, 2),
+                                 _stream(stream)),
+           "tp_conv_backward")
+    return dx, dw, dsh
+
+
+def tp_device_status(reset: bool = True, stream=None) -> int:
+    """Device status bits (TP_DEV_ERR_*); synchronises the stream."""
+    v = _i32()
+    _check(_lib.tp_device_status(ctypes.byref(v), int(bool(reset)), _stream(stream)), "tp_device_status")
+    return int(v.value)
+
+
+__all__ = ["Descriptor", "TPError", "LIB_PATH", "EXPORTS"] + EXPORTS

@@ -1,0 +1,171 @@
+// Device-side helpers: mbarrier / bulk-copy (TMA) / cp.async PTX wrappers,
+// the bounded pipeline wait, and bf16 unpacking. sm_100+ only.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tpconv.h"
+#include "tables.h"
+
+namespace tpc {
+
+// An mbarrier wait gives up after this long (nanoseconds of %globaltimer), so
+// a lost copy turns into a status bit instead of a hung GPU.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once all cp.async copies this thread issued so far have
+// landed (does not count as an extra expected arrival: .noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: true when the phase completed, false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on
+// `bar`. dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void set_status(int *status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// float value of element q of a row of T (float or bf16)
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+    static constexpr int kBytes = 4;
+};
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+};
+
+// Load CPT consecutive elements starting at p (aligned to CPT elements) as floats.
+template <int CPT>
+__device__ __forceinline__ void load_vec(const float *p, float (&v)[CPT]) {
+    if constexpr (CPT == 4) {
+        float4 t = *reinterpret_cast<const float4 *>(p);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else if constexpr (CPT == 2) {
+        float2 t = *reinterpret_cast<const float2 *>(p);
+        v[0] = t.x; v[1] = t.y;
+    } else {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) v[c] = p[c];
+    }
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int CPT>
+__device__ __forceinline__ void load_vec(const __nv_bfloat16 *p, float (&v)[CPT]) {
+    if constexpr (CPT == 4) {
+        uint2 t = *reinterpret_cast<const uint2 *>(p);
+        v[0] = bf16lo(t.x); v[1] = bf16hi(t.x); v[2] = bf16lo(t.y); v[3] = bf16hi(t.y);
+    } else if constexpr (CPT == 2) {
+        uint32_t t = *reinterpret_cast<const uint32_t *>(p);
+        v[0] = bf16lo(t); v[1] = bf16hi(t);
+    } else {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) v[c] = __bfloat162float(p[c]);
+    }
+}
+
+template <int CPT>
+__device__ __forceinline__ void store_vec(float *p, const float (&v)[CPT]) {
+    if constexpr (CPT == 4) {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    } else if constexpr (CPT == 2) {
+        *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) p[c] = v[c];
+    }
+}
+
+// Copy the parts of the tables the kernels read into shared memory.
+struct SmemTables {
+    uint16_t rec_ptr[kMaxM + 1];
+    uint16_t rec_j[kMaxTerms];
+    float rec_c[kMaxTerms];
+};
+
+}  // namespace tpc

@@ -1,0 +1,331 @@
+// Host-side descriptor builder: irreps strings -> path table, real
+// Clebsch-Gordan tensors and the kernel tables (tables.h).
+//
+// Irreps grammar and dims: Lesson 12a: Foundations of cuEquivariance,
+// section 21.2. Path rule and weight order: section 21.4 (channelwise
+// "uvu" paths filtered by the requested output types). The real
+// Clebsch-Gordan tensors are derived here from Racah's closed formula for
+// the complex coefficients <l1 m1 l2 m2 | l3 m3>, mapped to the real basis
+// (m = -l..l, z pole, cos-type for m > 0, sin-type for m < 0) by the unitary
+// U_l with Y_real = U_l Y_complex:
+//     C[i,j,k] = sum U3[k,M] <l1 m1 l2 m2|l3 M> conj(U1[i,m1]) conj(U2[j,m2]),
+// which is real up to one global phase; the phase is dropped, the tensor is
+// scaled to be orthonormal over (i,j) for each k and its sign fixed so the
+// first entry above 1e-9 in (i,j,k) row-major order is positive.
+#include <cctype>
+#include <cmath>
+#include <complex>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/tpconv.h"
+#include "tables.h"
+
+namespace {
+
+struct Term {
+    int mul, l, p;
+};
+
+// Parse "32x0e + 32x1o" / "0+1+2". Returns false on a malformed string.
+bool parse_irreps(const char *s, std::vector<Term> &out) {
+    out.clear();
+    std::string body;
+    for (const char *c = s; *c; ++c)
+        if (!std::isspace(static_cast<unsigned char>(*c))) body.push_back(*c);
+    if (body.empty()) return false;
+    int with_parity = 0, without = 0;
+    size_t pos = 0;
+    while (pos <= body.size()) {
+        size_t plus = body.find('+', pos);
+        std::string t = body.substr(pos, plus == std::string::npos ? std::string::npos : plus - pos);
+        if (t.empty()) return false;
+        Term term{1, 0, 0};
+        size_t x = t.find('x');
+        std::string lp = t;
+        if (x != std::string::npos) {
+            std::string m = t.substr(0, x);
+            if (m.empty() || m.size() > 6) return false;
+            for (char ch : m)
+                if (!std::isdigit(static_cast<unsigned char>(ch))) return false;
+            term.mul = std::atoi(m.c_str());
+            lp = t.substr(x + 1);
+        }
+        if (lp.empty()) return false;
+        char last = lp.back();
+        if (last == 'e' || last == 'o') {
+            term.p = last == 'e' ? 1 : -1;
+            lp.pop_back();
+            ++with_parity;
+        } else {
+            ++without;
+        }
+        if (lp.empty() || lp.size() > 3) return false;
+        for (char ch : lp)
+            if (!std::isdigit(static_cast<unsigned char>(ch))) return false;
+        term.l = std::atoi(lp.c_str());
+        out.push_back(term);
+        if (plus == std::string::npos) break;
+        pos = plus + 1;
+    }
+    return !(with_parity && without);
+}
+
+double fact(int n) {
+    double r = 1.0;
+    for (int i = 2; i <= n; ++i) r *= i;
+    return r;
+}
+
+// <j1 m1 j2 m2 | J M>, Racah's formula.
+double cg_complex(int j1, int m1, int j2, int m2, int J, int M) {
+    if (M != m1 + m2 || J < std::abs(j1 - j2) || J > j1 + j2) return 0.0;
+    if (std::abs(m1) > j1 || std::abs(m2) > j2 || std::abs(M) > J) return 0.0;
+    double pre = std::sqrt((2.0 * J + 1.0) * fact(J + j1 - j2) * fact(J - j1 + j2) * fact(j1 + j2 - J) /
+                           fact(j1 + j2 + J + 1));
+    pre *= std::sqrt(fact(J + M) * fact(J - M) * fact(j1 - m1) * fact(j1 + m1) * fact(j2 - m2) * fact(j2 + m2));
+    double s = 0.0;
+    for (int k = 0; k <= j1 + j2 + J + 1; ++k) {
+        int a[6] = {k, j1 + j2 - J - k, j1 - m1 - k, j2 + m2 - k, J - j2 + m1 + k, J - j1 - m2 + k};
+        bool ok = true;
+        for (int v : a) ok = ok && v >= 0;
+        if (!ok) continue;
+        double den = 1.0;
+        for (int v : a) den *= fact(v);
+        s += ((k & 1) ? -1.0 : 1.0) / den;
+    }
+    return pre * s;
+}
+
+// U_l[row = m+l][col = m'+l]: real harmonic m as a combination of complex m'.
+std::vector<std::complex<double>> real_basis(int l) {
+    const int n = 2 * l + 1;
+    std::vector<std::complex<double>> u(n * n, 0.0);
+    const double r2 = 1.0 / std::sqrt(2.0);
+    for (int m = -l; m <= l; ++m) {
+        const int row = m + l;
+        if (m > 0) {
+            u[row * n + (m + l)] = ((m & 1) ? -r2 : r2);
+            u[row * n + (-m + l)] = r2;
+        } else if (m < 0) {
+            const int mu = -m;
+            u[row * n + (-mu + l)] = std::complex<double>(0.0, r2);
+            u[row * n + (mu + l)] = std::complex<double>(0.0, (mu & 1) ? r2 : -r2);
+        } else {
+            u[row * n + l] = 1.0;
+        }
+    }
+    return u;
+}
+
+void real_cg(int l1, int l2, int l3, double *C) {
+    const int n1 = 2 * l1 + 1, n2 = 2 * l2 + 1, n3 = 2 * l3 + 1;
+    auto U1 = real_basis(l1), U2 = real_basis(l2), U3 = real_basis(l3);
+    std::vector<std::complex<double>> T(n1 * n2 * n3, 0.0);
+    for (int i = 0; i < n1; ++i)
+        for (int j = 0; j < n2; ++j)
+            for (int k = 0; k < n3; ++k) {
+                std::complex<double> acc = 0.0;
+                for (int m1 = -l1; m1 <= l1; ++m1) {
+                    const auto a = std::conj(U1[i * n1 + (m1 + l1)]);
+                    if (a == 0.0) continue;
+                    for (int m2 = -l2; m2 <= l2; ++m2) {
+                        const auto b = std::conj(U2[j * n2 + (m2 + l2)]);
+                        if (b == 0.0) continue;
+                        const int M = m1 + m2;
+                        if (std::abs(M) > l3) continue;
+                        const auto c = U3[k * n3 + (M + l3)];
+                        if (c == 0.0) continue;
+                        acc += c * a * b * cg_complex(l1, m1, l2, m2, l3, M);
+                    }
+                }
+                T[(i * n2 + j) * n3 + k] = acc;
+            }
+    double nre = 0.0, nim = 0.0;
+    for (auto &t : T) {
+        nre += t.real() * t.real();
+        nim += t.imag() * t.imag();
+    }
+    const bool use_re = nre >= nim;
+    double norm2 = 0.0;
+    for (size_t q = 0; q < T.size(); ++q) {
+        C[q] = use_re ? T[q].real() : T[q].imag();
+        norm2 += C[q] * C[q];
+    }
+    const double scale = norm2 > 0 ? std::sqrt(n3 / norm2) : 0.0;
+    double sign = 0.0;
+    for (size_t q = 0; q < T.size(); ++q) {
+        C[q] *= scale;
+        if (std::fabs(C[q]) < 1e-12) C[q] = 0.0;
+        if (sign == 0.0 && std::fabs(C[q]) > 1e-9) sign = C[q] > 0 ? 1.0 : -1.0;
+    }
+    for (size_t q = 0; q < T.size(); ++q) C[q] *= sign;
+}
+
+void free_desc(tp_desc *d) {
+    if (!d) return;
+    for (int p = 0; p < d->n_paths; ++p) std::free(d->cg[p]);
+    delete d;
+}
+
+}  // namespace
+
+extern "C" tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh, const char *irreps_out,
+                                    tp_layout layout, tp_desc **out) {
+    using namespace tpc;
+    if (!irreps_in || !irreps_sh || !irreps_out || !out) return TP_ERR_ARG;
+    *out = nullptr;
+    std::vector<Term> tin, tsh, tout;
+    if (!parse_irreps(irreps_in, tin) || !parse_irreps(irreps_sh, tsh) || !parse_irreps(irreps_out, tout))
+        return TP_ERR_PARSE;
+    if (layout == TP_MUL_IR) return TP_ERR_UNSUPPORTED;
+    if (layout != TP_IR_MUL) return TP_ERR_ARG;
+    // O3 vs SO3 must agree across the three strings
+    auto kind = [](const std::vector<Term> &v) { return v[0].p != 0; };
+    if (kind(tin) != kind(tsh) || kind(tin) != kind(tout)) return TP_ERR_PARSE;
+    if (tin.size() > 4 || tout.size() > 4 || tsh.size() > (size_t)kMaxShBlocks) return TP_ERR_UNSUPPORTED;
+
+    tp_desc *d = new (std::nothrow) tp_desc();
+    if (!d) return TP_ERR_ARG;
+    std::memset(d, 0, sizeof(*d));
+    d->n_in = (int)tin.size();
+    d->n_sh = (int)tsh.size();
+    d->n_out = (int)tout.size();
+    int mul = tin[0].mul;
+    bool seen_in[4] = {false, false, false, false}, seen_out[4] = {false, false, false, false};
+    int off = 0;
+    d->lmax_in = d->lmax_sh = d->lmax_out = 0;
+    for (int a = 0; a < d->n_in; ++a) {
+        const Term &t = tin[a];
+        if (t.l > kMaxL || t.mul != mul || seen_in[t.l]) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+        seen_in[t.l] = true;
+        d->in_mul[a] = t.mul; d->in_l[a] = t.l; d->in_p[a] = t.p; d->in_off[a] = off;
+        off += t.mul * (2 * t.l + 1);
+        if (t.l > d->lmax_in) d->lmax_in = t.l;
+    }
+    const int dim_x = off;
+    off = 0;
+    for (int b = 0; b < d->n_sh; ++b) {
+        const Term &t = tsh[b];
+        if (t.l > kMaxL || t.mul != 1) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+        d->sh_l[b] = t.l; d->sh_p[b] = t.p; d->sh_off[b] = off;
+        off += 2 * t.l + 1;
+        if (t.l > d->lmax_sh) d->lmax_sh = t.l;
+    }
+    const int dim_sh = off;
+    off = 0;
+    for (int c = 0; c < d->n_out; ++c) {
+        const Term &t = tout[c];
+        if (t.l > kMaxL || t.mul != mul || seen_out[t.l]) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+        seen_out[t.l] = true;
+        d->out_mul[c] = t.mul; d->out_l[c] = t.l; d->out_p[c] = t.p; d->out_off[c] = off;
+        off += t.mul * (2 * t.l + 1);
+        if (t.l > d->lmax_out) d->lmax_out = t.l;
+    }
+    const int dim_out = off;
+    if (mul % 8 != 0 || mul > 128 || mul <= 0 || dim_sh > kMaxSh) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+
+    // paths: a-major, then b, then l_o ascending (triangle rule, parity product)
+    int np = 0;
+    for (int a = 0; a < d->n_in; ++a)
+        for (int b = 0; b < d->n_sh; ++b)
+            for (int lo = std::abs(d->in_l[a] - d->sh_l[b]); lo <= d->in_l[a] + d->sh_l[b]; ++lo) {
+                const int po = d->in_p[a] * d->sh_p[b];
+                for (int c = 0; c < d->n_out; ++c) {
+                    if (d->out_l[c] != lo || d->out_p[c] != po) continue;
+                    if (np >= kMaxPaths) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+                    d->path_a[np] = a; d->path_b[np] = b; d->path_c[np] = c;
+                    const int n1 = 2 * d->in_l[a] + 1, n2 = 2 * d->sh_l[b] + 1, n3 = 2 * lo + 1;
+                    d->cg[np] = static_cast<double *>(std::malloc(sizeof(double) * n1 * n2 * n3));
+                    if (!d->cg[np]) { free_desc(d); return TP_ERR_ARG; }
+                    d->n_paths = np + 1;
+                    real_cg(d->in_l[a], d->sh_l[b], lo, d->cg[np]);
+                    ++np;
+                }
+            }
+    d->n_paths = np;
+    if (np == 0) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+
+    // kernel tables
+    Tables &T = d->tab;
+    T.n_paths = np; T.mul = mul; T.dim_x = dim_x; T.dim_sh = dim_sh; T.dim_out = dim_out;
+    T.wnum = np * mul;
+    for (int l = 0; l < 4; ++l) { T.x_off[l] = -1; T.o_off[l] = -1; }
+    for (int a = 0; a < d->n_in; ++a) T.x_off[d->in_l[a]] = d->in_off[a];
+    for (int c = 0; c < d->n_out; ++c) T.o_off[d->out_l[c]] = d->out_off[c];
+    T.n_sh_blocks = d->n_sh;
+    for (int b = 0; b < d->n_sh; ++b) T.sh_l[b] = (uint8_t)d->sh_l[b];
+    int R = 0, nnz = 0;
+    std::vector<std::vector<std::pair<int, float>>> col(dim_sh);  // transposed recipe
+    for (int p = 0; p < np; ++p) {
+        const int la = d->in_l[d->path_a[p]], lb = d->sh_l[d->path_b[p]], lc = d->out_l[d->path_c[p]];
+        const int n1 = 2 * la + 1, n2 = 2 * lb + 1, n3 = 2 * lc + 1;
+        T.la[p] = (uint8_t)la; T.lb[p] = (uint8_t)lb; T.lc[p] = (uint8_t)lc;
+        T.m_off[p] = (uint16_t)R;
+        const int padded = (n1 * n3 + 3) / 4 * 4;
+        if (R + padded > kMaxM) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+        for (int q = 0; q < padded; ++q) {
+            T.rec_ptr[R + q] = (uint16_t)nnz;
+            if (q < n1 * n3) {
+                const int i = q / n3, k = q % n3;
+                for (int j = 0; j < n2; ++j) {
+                    const double c = d->cg[p][(i * n2 + j) * n3 + k];
+                    if (c == 0.0) continue;
+                    if (nnz >= kMaxTerms) { free_desc(d); return TP_ERR_UNSUPPORTED; }
+                    const int jg = d->sh_off[d->path_b[p]] + j;
+                    T.rec_j[nnz] = (uint16_t)jg;
+                    T.rec_c[nnz] = (float)c;
+                    col[jg].push_back({R + q, (float)c});
+                    ++nnz;
+                }
+            }
+        }
+        R += padded;
+    }
+    T.rec_ptr[R] = (uint16_t)nnz;
+    T.R = R;
+    T.nnz = nnz;
+    int t = 0;
+    for (int j = 0; j < dim_sh; ++j) {
+        T.tr_ptr[j] = (uint16_t)t;
+        for (auto &e : col[j]) { T.tr_r[t] = (uint16_t)e.first; T.tr_c[t] = e.second; ++t; }
+    }
+    T.tr_ptr[dim_sh] = (uint16_t)t;
+    *out = d;
+    return TP_OK;
+}
+
+extern "C" tp_status tp_desc_query(const tp_desc *d, tp_desc_info *info) {
+    if (!d || !info) return TP_ERR_ARG;
+    info->n_paths = d->n_paths;
+    info->mul = d->tab.mul;
+    info->dim_x = d->tab.dim_x;
+    info->dim_sh = d->tab.dim_sh;
+    info->dim_out = d->tab.dim_out;
+    info->weight_numel = d->tab.wnum;
+    info->n_in = d->n_in; info->n_sh = d->n_sh; info->n_out = d->n_out;
+    info->lmax_in = d->lmax_in; info->lmax_sh = d->lmax_sh; info->lmax_out = d->lmax_out;
+    info->cg_nnz = d->tab.nnz;
+    return TP_OK;
+}
+
+extern "C" tp_status tp_desc_path(const tp_desc *d, int32_t p, tp_path_info *info) {
+    if (!d || !info || p < 0 || p >= d->n_paths) return TP_ERR_ARG;
+    info->a = d->path_a[p]; info->b = d->path_b[p]; info->c = d->path_c[p];
+    info->la = d->in_l[info->a]; info->lb = d->sh_l[info->b]; info->lc = d->out_l[info->c];
+    return TP_OK;
+}
+
+extern "C" tp_status tp_desc_cg(const tp_desc *d, int32_t p, double *out, int64_t capacity) {
+    if (!d || !out || p < 0 || p >= d->n_paths) return TP_ERR_ARG;
+    const int la = d->in_l[d->path_a[p]], lb = d->sh_l[d->path_b[p]], lc = d->out_l[d->path_c[p]];
+    const int64_t n = (int64_t)(2 * la + 1) * (2 * lb + 1) * (2 * lc + 1);
+    if (capacity < n) return TP_ERR_ARG;
+    std::memcpy(out, d->cg[p], sizeof(double) * n);
+    return TP_OK;
+}
+
+extern "C" void tp_desc_destroy(tp_desc *d) { free_desc(d); }

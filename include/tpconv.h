@@ -1,0 +1,195 @@
+/*
+ * tpconv.h - C ABI of the GB300 (sm_103a) fused equivariant tensor-product
+ * convolution library (libtpconv.so).
+ *
+ * What the library computes. For every edge e of a graph, gather the source
+ * node's irreps features x[src[e]], contract them with the edge's real
+ * spherical harmonics sh[e] through the real Clebsch-Gordan tensor C_p of
+ * every allowed path p = (l_a, l_b, l_c) in channelwise "uvu" mode, scale by
+ * the per-edge, per-path, per-channel weight w[e, p, u], and sum into the
+ * destination node:
+ *
+ *   out[d, c, k, u] = sum_{e: dst[e]=d} sum_{p=(a,b,c)} w[e,p,u]
+ *                     * sum_{i,j} C_p[i,j,k] x[src[e], a, i, u] sh[e, b, j]
+ *
+ * This is the descriptor "[ijk]·a[uv]·b[iu]·c[jv] -> D[kuv]" (v = 1) of
+ * Lesson 12a: Foundations of cuEquivariance, section 21.4, with the gather
+ * (input indices) and sum-scatter (output indices: repeated receivers sum,
+ * destinations without edges stay zero) of "cuEquivariance in PyTorch",
+ * SegmentedPolynomial: gather and scatter, and external per-edge weights
+ * (same page, Layouts and weights: a gathered graph op uses the edge count as
+ * the weight batch). All paths run in one kernel with no per-path
+ * intermediates (Lesson 12a, section 21.1).
+ *
+ * Conventions shared by every entry point:
+ *  - Feature rows use the ir_mul layout (Lesson 12a, section 21.3): block b of
+ *    multiplicity m and degree l occupies (2l+1)*m consecutive elements and
+ *    element (i, u) sits at off_b + i*m + u. Blocks follow the irreps string.
+ *  - Real basis: m = -l..l with the z axis as pole, l=1 ordered (y, z, x);
+ *    spherical harmonics with "component" normalisation (sum_m Y_lm^2 = 2l+1
+ *    on unit vectors). Clebsch-Gordan tensors are orthonormal over (i, j) for
+ *    each k, with the first nonzero entry in (i, j, k) row-major order
+ *    positive. No other normalisation factor is applied.
+ *  - Paths: for a in input blocks, b in harmonic blocks, l_o from |l_a-l_b| to
+ *    l_a+l_b ascending, kept when (l_o, p_a*p_b) is one of the output types
+ *    (Lesson 12a, section 21.4). Paths reaching the same output type sum into
+ *    that one output block. Weights are w[e, p*mul + u], path-major.
+ *  - Pointers named "device" must be device memory of the current CUDA device;
+ *    the caller allocates and owns every buffer. The library owns only the
+ *    opaque descriptor (host memory). Every GPU entry point is asynchronous on
+ *    `stream` (a cudaStream_t; NULL = legacy default stream) and returns a
+ *    host-side status for argument errors and launch failures. Problems found
+ *    on the device (index out of range, a pipeline wait that gave up) set bits
+ *    of a per-device status word read with tp_device_status(); kernels never
+ *    trap.
+ *  - Indices are int32. Edge counts must be < 2^31.
+ */
+#ifndef TPCONV_H
+#define TPCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TPCONV_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define TPCONV_API __attribute__((visibility("default")))
+#else
+#define TPCONV_API
+#endif
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_PARSE = 1,       /* an irreps string cannot be parsed */
+    TP_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (see tp_desc_create) */
+    TP_ERR_UNSORTED = 3,    /* row pointers not non-decreasing / not ending at E */
+    TP_ERR_INDEX = 4,       /* an index is out of range */
+    TP_ERR_ALIGN = 5,       /* a pointer or row size breaks the 16-byte rule */
+    TP_ERR_CUDA = 6,        /* a CUDA runtime call failed */
+    TP_ERR_ARG = 7,         /* null pointer, negative size or bad enum */
+    TP_ERR_TIMEOUT = 8      /* a device pipeline wait gave up (device status bit) */
+} tp_status;
+
+typedef enum { TP_IR_MUL = 0, TP_MUL_IR = 1 } tp_layout;
+
+typedef enum {
+    TP_F32 = 0,           /* x, w float32; math and out float32 */
+    TP_BF16_IN_F32_OUT = 1 /* x, w bfloat16; math (fp32 accumulation) and out float32 */
+} tp_dtype;
+
+/* device status bits (tp_device_status) */
+#define TP_DEV_ERR_INDEX 0x1   /* src/dst/key outside [0, N) - the edge was skipped */
+#define TP_DEV_ERR_TIMEOUT 0x2 /* an mbarrier wait exceeded its iteration limit */
+#define TP_DEV_ERR_SEGMENT 0x4 /* row pointers not non-decreasing or outside [0, E] */
+
+typedef struct tp_desc tp_desc;
+
+typedef struct {
+    int32_t n_paths;       /* P */
+    int32_t mul;           /* channel multiplicity u (uniform) */
+    int32_t dim_x;         /* sum over input blocks of mul*(2l+1) */
+    int32_t dim_sh;        /* sum over harmonic blocks of (2l+1) */
+    int32_t dim_out;       /* sum over output blocks of mul*(2l+1) */
+    int32_t weight_numel;  /* P*mul */
+    int32_t n_in, n_sh, n_out; /* number of blocks */
+    int32_t lmax_in, lmax_sh, lmax_out;
+    int32_t cg_nnz;        /* nonzero Clebsch-Gordan entries over all paths */
+} tp_desc_info;
+
+typedef struct {
+    int32_t a, b, c;    /* block indices into irreps_in, irreps_sh, irreps_out */
+    int32_t la, lb, lc; /* their degrees */
+} tp_path_info;
+
+/* Build a descriptor from three irreps strings ("128x0e+128x1o+128x2e",
+ * "0e+1o+2e+3o", ...; O(3) with e/o parity letters or SO(3) without,
+ * Lesson 12a, section 21.2). The host derives the path table, the real
+ * Clebsch-Gordan tensors (Racah's formula in the complex basis, then the
+ * complex-to-real change of basis) and the kernel tables.
+ * Errors: TP_ERR_PARSE for a malformed string; TP_ERR_UNSUPPORTED when
+ * layout != TP_IR_MUL, a degree exceeds 3, a harmonic block has mul != 1,
+ * input/output multiplicities differ or are not one value, an output type
+ * repeats, two input (or output) blocks share a degree, mul is not a
+ * multiple of 8 or exceeds 128, or no path exists; TP_ERR_ARG for nulls.
+ * On success *out owns host memory until tp_desc_destroy. */
+TPCONV_API tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh, const char *irreps_out,
+                         tp_layout layout, tp_desc **out);
+TPCONV_API tp_status tp_desc_query(const tp_desc *desc, tp_desc_info *info);
+/* Path p in enumeration order (the weight layout order). */
+TPCONV_API tp_status tp_desc_path(const tp_desc *desc, int32_t p, tp_path_info *info);
+/* Copy path p's dense Clebsch-Gordan tensor [2la+1][2lb+1][2lc+1] (row-major,
+ * float64) into host memory `out` of `capacity` doubles. */
+TPCONV_API tp_status tp_desc_cg(const tp_desc *desc, int32_t p, double *out, int64_t capacity);
+TPCONV_API void tp_desc_destroy(tp_desc *desc);
+
+/* Real spherical harmonics of the desc's harmonic irreps for E edge vectors
+ * ("cuEquivariance in PyTorch", Spherical harmonics and a NumPy reference:
+ * normalize != 0 first scales each vector to unit length; normalize == 0
+ * evaluates the raw homogeneous polynomial).
+ * vec: device float32 [E][3]; sh: device float32 [E][dim_sh]. */
+TPCONV_API tp_status tp_spherical_harmonics(const tp_desc *desc, const float *vec, int64_t E, int32_t normalize,
+                                 float *sh, void *stream);
+
+/* Workspace bytes tp_csr_build needs for E keys in [0, N). */
+TPCONV_API tp_status tp_csr_workspace_size(int64_t E, int32_t N, size_t *bytes);
+
+/* Stable counting sort of keys (a dst-sorted CSR when keys = dst; a source
+ * CSR for the backward when keys = src in dst-sorted edge order).
+ * keys: device int32 [E] in [0, N). Outputs (device, caller-owned):
+ *   perm[E]         perm[k] = original position of the k-th sorted key; equal
+ *                   keys keep their original order;
+ *   row_ptr[N+1]    row_ptr[0] = 0, row_ptr[N] = E, segment d = [row_ptr[d], row_ptr[d+1]);
+ *   keys_sorted[E]  optional (NULL to skip).
+ * workspace: device memory of at least tp_csr_workspace_size bytes, 256-byte
+ * aligned. Keys outside [0, N) set TP_DEV_ERR_INDEX; outputs are then
+ * unspecified but every write stays inside the output arrays. */
+TPCONV_API tp_status tp_csr_build(const int32_t *keys, int64_t E, int32_t N, int32_t *perm, int32_t *row_ptr,
+                       int32_t *keys_sorted, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Forward pass (the hot path). Edges must be in destination-sorted order with
+ * row_ptr[N_dst+1] from tp_csr_build (edge range of destination d is
+ * [row_ptr[d], row_ptr[d+1])).
+ *   x:   device [N_src][dim_x], float32 (TP_F32) or bfloat16 (TP_BF16_IN_F32_OUT), ir_mul;
+ *   sh:  device float32 [E][dim_sh];
+ *   w:   device [E][weight_numel], same type as x;
+ *   src: device int32 [E], in [0, N_src);
+ *   out: device float32 [N_dst][dim_out], fully overwritten (zero rows for
+ *        destinations without edges).
+ * x, w and out must be 16-byte aligned; dim_x*sizeof(x) and
+ * weight_numel*sizeof(w) must be multiples of 16 (they are whenever mul % 8
+ * == 0). Out-of-range src entries are skipped and set TP_DEV_ERR_INDEX.
+ * Summation order is fixed: results are bitwise reproducible run to run. */
+TPCONV_API tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const void *x, const float *sh,
+                          const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src,
+                          int32_t N_dst, int64_t E, float *out, void *stream);
+
+/* Backward pass of tp_conv_forward (float32), the exact gradients of
+ * <grad_out, out> with respect to x, w and sh:
+ *   dx[s,a,i,u] = sum_{e: src[e]=s} sum_{p: a_p=a} w[e,p,u] sum_{j,k} C_p[i,j,k] sh[e,b,j] g[dst[e],c,k,u]
+ *   dw[e,p,u]   = sum_{i,j,k} C_p[i,j,k] x[src[e],a,i,u] sh[e,b,j] g[dst[e],c,k,u]
+ *   dsh[e,b,j]  = sum_{p: b_p=b} sum_{i,k,u} C_p[i,j,k] x[src[e],a,i,u] w[e,p,u] g[dst[e],c,k,u]
+ * Edges are in destination-sorted order (row_ptr as for the forward; dst[E]
+ * the sorted destination of each edge). The source CSR (src_perm, src_row_ptr)
+ * is tp_csr_build of `src` in that same edge order: src_perm lists edge
+ * positions grouped by source. dx [N_src][dim_x], dw [E][weight_numel] and
+ * dsh [E][dim_sh] are fully overwritten. Deterministic (no atomics). */
+TPCONV_API tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out, const float *x, const float *sh,
+                           const float *w, const int32_t *src, const int32_t *dst, const int32_t *row_ptr,
+                           const int32_t *src_perm, const int32_t *src_row_ptr, int32_t N_src,
+                           int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh, void *stream);
+
+/* Read (and, when reset != 0, clear) the current device's status word into
+ * *flags (TP_DEV_ERR_* bits). Synchronises `stream`. */
+TPCONV_API tp_status tp_device_status(int32_t *flags, int32_t reset, void *stream);
+
+TPCONV_API const char *tp_status_string(tp_status status);
+TPCONV_API int32_t tp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TPCONV_H */

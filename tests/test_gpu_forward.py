@@ -1,0 +1,150 @@
+"""GPU parity of tp_conv_forward against the fp64 oracle, element by element,
+on seeded problems that span several chunks and warps with ragged tails, every
+kernel shape and channel width, and the edge cases of the method (empty graph,
+destinations without edges, unreachable output blocks, bipartite graphs,
+out-of-range sources), plus run-to-run bitwise determinism."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import deg_tol, BF16_TOL, FP32_TOL, dev_tensor, err, gpu_sorted_inputs, make_problem, oracle_forward
+from oracle import tp
+from workloads import WORKLOADS, make_features, make_graph
+
+pytestmark = pytest.mark.gpu
+
+
+def run(tpc, prob, dtype=torch.float32):
+    desc = tpc.tp_desc_create(*prob["irreps"])
+    g = gpu_sorted_inputs(tpc, prob, dtype)
+    out = tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], g["row_ptr"], prob["n_dst"])
+    torch.cuda.synchronize()
+    return out, desc, g
+
+
+SHAPES = [
+    ("32x0e+32x1o", "0e+1o+2e", "32x0e+32x1o+32x2e"),              # tiny / very large workloads
+    ("128x0e+128x1o+128x2e", "0e+1o+2e+3o", "128x0e+128x1o+128x2e"),  # medium / fwd+bwd
+    ("64x0e+64x1o+64x2e+64x3o", "0e+1o+2e+3o", "64x0e+64x1o+64x2e+64x3o"),  # large
+    ("32x0e+32x1o", "0e+1o", "32x0e+32x1o"),                        # the lesson's worked example
+    ("16x0+16x1+16x2", "0+1+2", "16x0+16x1+16x2"),                  # SO(3)
+    ("8x0e+8x1o", "0e+1o+2e+3o", "8x0e+8x1o+8x2e+8x3o"),            # mul 8: most lanes idle
+    ("40x2e+40x0e", "1o+0e+2e", "40x1o+40x2e+40x0e"),               # block order, mul 40
+    ("96x1o", "0e+1o+2e", "96x0e+96x1e+96x2e"),                     # single input block, mul 96
+    ("24x0e+24x2e", "0e+2e", "24x0e+24x2e+24x3o"),                  # missing degree, unreachable 3o
+]
+
+
+@pytest.mark.parametrize("irr", SHAPES, ids=lambda c: "|".join(c))
+def test_forward_matches_oracle(tpc, irr):
+    prob = make_problem(*irr, n_src=300, n_dst=257, E=5000, seed=1)
+    out, _, _ = run(tpc, prob)
+    ref = oracle_forward(prob)
+    assert err(out, ref) <= FP32_TOL
+    assert tpc.tp_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("irr", SHAPES[:3], ids=lambda c: "|".join(c))
+def test_forward_bf16_inputs(tpc, irr):
+    prob = make_problem(*irr, n_src=200, n_dst=190, E=3000, seed=2)
+    out, _, _ = run(tpc, prob, torch.bfloat16)
+    ref = oracle_forward(prob, torch.bfloat16)
+    e = err(out, ref)
+    assert e <= BF16_TOL
+    assert e <= FP32_TOL   # fp32 math on the same rounded inputs
+
+
+def test_tiny_workload(tpc):
+    wl = WORKLOADS["tiny"]
+    rng, src, dst, vec, n = make_graph(wl)
+    prob = make_problem(wl.irreps_in, wl.irreps_sh, wl.irreps_out, n, n, len(src), src=src, dst=dst)
+    pl = prob["plan"]
+    x, w, _ = make_features(rng, wl, n, len(src), pl.dim_in, pl.weight_numel, pl.n_paths, pl.dim_out)
+    from oracle import so3
+    prob.update(x=x, w=w, sh=so3.sh_concat([t.l for t in pl.irr_sh], vec))
+    out, _, _ = run(tpc, prob)
+    assert err(out, oracle_forward(prob)) <= FP32_TOL
+
+
+def test_degree_extremes_and_empty_rows(tpc):
+    """One destination with 1000 edges (many chunks), many with none, a ragged mix."""
+    rng = np.random.default_rng(5)
+    n_dst = 700
+    dst = np.concatenate([np.full(1000, 3), rng.integers(0, n_dst // 2, 3000) * 2, [n_dst - 1]])
+    rng.shuffle(dst)
+    prob = make_problem(*SHAPES[1], n_src=50, n_dst=n_dst, E=len(dst), seed=6, dst=dst)
+    out, _, _ = run(tpc, prob)
+    ref = oracle_forward(prob)
+    # destination 3 sums 1000 edges: judge every row against its own RMS (the
+    # whole-tensor RMS, diluted by empty rows, understates its magnitude)
+    on = out.double().cpu().numpy()
+    for d, c in zip(*np.unique(dst, return_counts=True)):
+        assert err(on[d], ref[d]) <= deg_tol(c), d
+    empty = np.setdiff1d(np.arange(n_dst), dst)
+    assert len(empty) > 100 and not out[torch.as_tensor(empty)].any()
+
+
+def test_empty_graph_zeroes_output(tpc):
+    prob = make_problem(*SHAPES[0], n_src=10, n_dst=33, E=0, seed=0)
+    desc = tpc.tp_desc_create(*prob["irreps"])
+    out = torch.full((33, desc.dim_out), 7.0, device="cuda")
+    z = torch.zeros(0, device="cuda")
+    row_ptr = torch.zeros(34, dtype=torch.int32, device="cuda")
+    tpc.tp_conv_forward(desc, torch.zeros((10, desc.dim_x), device="cuda"), z.view(0, desc.dim_sh),
+                        torch.zeros((0, desc.weight_numel), device="cuda"), torch.zeros(0, dtype=torch.int32,
+                                                                                      device="cuda"),
+                        row_ptr, 33, out=out)
+    torch.cuda.synchronize()
+    assert not out.any()
+
+
+def test_bipartite_sources(tpc):
+    """The gather/scatter example's shape: more sources than destinations."""
+    prob = make_problem(*SHAPES[3], n_src=5000, n_dst=40, E=3000, seed=9)
+    out, _, _ = run(tpc, prob)
+    assert err(out, oracle_forward(prob)) <= FP32_TOL
+    prob = make_problem(*SHAPES[3], n_src=3, n_dst=900, E=3000, seed=10)
+    out, _, _ = run(tpc, prob)
+    assert err(out, oracle_forward(prob)) <= FP32_TOL
+
+
+def test_deterministic(tpc):
+    prob = make_problem(*SHAPES[2], n_src=500, n_dst=480, E=16000, seed=11)
+    desc = tpc.tp_desc_create(*prob["irreps"])
+    g = gpu_sorted_inputs(tpc, prob)
+    a = tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], g["row_ptr"], prob["n_dst"])
+    b = tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], g["row_ptr"], prob["n_dst"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_out_of_range_source_is_skipped_and_flagged(tpc):
+    prob = make_problem(*SHAPES[0], n_src=64, n_dst=64, E=2000, seed=12)
+    desc = tpc.tp_desc_create(*prob["irreps"])
+    g = gpu_sorted_inputs(tpc, prob)
+    bad = g["src"].clone()
+    bad[17] = 64
+    bad[1000] = -5
+    out = tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], bad, g["row_ptr"], 64)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) & tpc.TP_DEV_ERR_INDEX
+    # the other edges are unaffected: compare with the oracle minus the two bad edges
+    keep = np.ones(2000, bool)
+    perm = g["perm"].cpu().numpy()
+    keep[perm[[17, 1000]]] = False
+    sub = dict(prob)
+    sub.update(src=prob["src"][keep], dst=prob["dst"][keep], sh=prob["sh"][keep], w=prob["w"][keep])
+    assert err(out, oracle_forward(sub)) <= FP32_TOL
+    assert tpc.tp_device_status(reset=True) == 0
+
+
+def test_bad_row_pointers_flagged(tpc):
+    prob = make_problem(*SHAPES[0], n_src=64, n_dst=64, E=2000, seed=13)
+    desc = tpc.tp_desc_create(*prob["irreps"])
+    g = gpu_sorted_inputs(tpc, prob)
+    rp = g["row_ptr"].clone()
+    rp[10] = 5000          # beyond E
+    rp[20] = rp[19] - 1    # decreasing
+    tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], rp, 64)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) & tpc.TP_DEV_ERR_SEGMENT

@@ -1,0 +1,102 @@
+"""Host-side checks of the C-ABI library (no GPU needed): every symbol the
+header declares is exported, the descriptor builder (Racah-formula
+Clebsch-Gordan tensors, path table) agrees with the independent oracle, and
+argument errors come back as status codes without touching a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import tp
+from workloads import WORKLOADS
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tpconv.h")
+
+
+def header_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"TPCONV_API\s+(?:const\s+)?\w+\s*\*?\s*(tp_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(tpc):
+    names = header_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(tpc._lib, n), n
+    assert set(names) == set(tpc.EXPORTS)
+    assert tpc.tp_abi_version() == 1
+    assert tpc.tp_status_string(4) == "index out of range"
+
+
+CONFIGS = [(w.irreps_in, w.irreps_sh, w.irreps_out) for w in WORKLOADS.values()] + [
+    ("32x0e+32x1o", "0e+1o", "32x0e+32x1o"),
+    ("16x0+16x1+16x2", "0+1+2+3", "16x0+16x1+16x2+16x3"),
+    ("8x2e+8x0e", "1o+0e", "8x1o+8x2e+8x3o"),
+    ("24x1o", "0e+1o+2e", "24x0e+24x1e+24x2e"),
+]
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=lambda c: "|".join(c))
+def test_descriptor_matches_oracle(tpc, cfg):
+    d = tpc.tp_desc_create(*cfg)
+    pl = tp.Plan(*cfg)
+    assert (d.n_paths, d.mul, d.dim_x, d.dim_sh, d.dim_out, d.weight_numel) == \
+        (pl.n_paths, pl.mul, pl.dim_in, pl.dim_sh, pl.dim_out, pl.weight_numel)
+    nnz = 0
+    for p in range(d.n_paths):
+        P = pl.paths[p]
+        assert tpc.tp_desc_path(d, p) == (P.a, P.b, P.c, P.la, P.lb, P.lc)
+        C = tpc.tp_desc_cg(d, p)
+        np.testing.assert_allclose(C, pl.cg[p], atol=1e-13)
+        nnz += int((pl.cg[p] != 0).sum())
+    assert d.cg_nnz == nnz
+
+
+@pytest.mark.parametrize("cfg,status", [
+    (("32x0e+32x1q", "0e", "32x0e"), "TP_ERR_PARSE"),
+    (("32x0e+", "0e", "32x0e"), "TP_ERR_PARSE"),
+    (("32x0e", "0", "32x0e"), "TP_ERR_PARSE"),             # O3 vs SO3 mismatch
+    (("32x4e", "0e", "32x4e"), "TP_ERR_UNSUPPORTED"),      # l > 3
+    (("32x0e", "2x0e", "32x0e"), "TP_ERR_UNSUPPORTED"),    # harmonic multiplicity
+    (("32x0e", "0e", "16x0e"), "TP_ERR_UNSUPPORTED"),      # uvu multiplicity
+    (("12x0e", "0e", "12x0e"), "TP_ERR_UNSUPPORTED"),      # mul % 8
+    (("256x0e", "0e", "256x0e"), "TP_ERR_UNSUPPORTED"),    # mul > 128
+    (("32x0e", "1o", "32x0e"), "TP_ERR_UNSUPPORTED"),      # no path
+    (("32x0e+32x0o", "0e", "32x0e+32x0o"), "TP_ERR_UNSUPPORTED"),  # two input blocks of one degree
+    (("24x1o", "0e+1o", "24x1o+24x1e"), "TP_ERR_UNSUPPORTED"),     # two output blocks of one degree
+])
+def test_descriptor_errors(tpc, cfg, status):
+    with pytest.raises(tpc.TPError) as ei:
+        tpc.tp_desc_create(*cfg)
+    assert tpc.STATUS_NAMES[ei.value.status] == status
+    with pytest.raises(tpc.TPError):
+        tpc.tp_desc_create("32x0e", "0e", "32x0e", layout="mul_ir")
+
+
+def test_argument_errors_need_no_gpu(tpc):
+    """Validation happens before any CUDA call: bogus pointers are never touched."""
+    lib = tpc._lib
+    d = tpc.tp_desc_create("32x0e+32x1o", "0e+1o+2e", "32x0e+32x1o+32x2e")
+    vp = ctypes.c_void_p
+    good, odd = vp(0x10000), vp(0x10004)
+    # null out / row_ptr
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, vp(0), 4, 4, 10, good, vp(0)) == 7
+    # misaligned x
+    assert lib.tp_conv_forward(d.handle, 0, odd, good, good, good, good, 4, 4, 10, good, vp(0)) == 5
+    # negative sizes, bad dtype, E >= 2^31
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, -1, 4, 10, good, vp(0)) == 7
+    assert lib.tp_conv_forward(d.handle, 5, good, good, good, good, good, 4, 4, 10, good, vp(0)) == 7
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, 4, 4, 1 << 31, good, vp(0)) == 7
+    # edges but no source nodes
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, 0, 4, 10, good, vp(0)) == 4
+    # no destinations: nothing to do
+    assert lib.tp_conv_forward(d.handle, 0, vp(0), vp(0), vp(0), vp(0), vp(0), 0, 0, 0, vp(0), vp(0)) == 0
+    n = ctypes.c_size_t()
+    assert lib.tp_csr_workspace_size(1000, 50, ctypes.byref(n)) == 0 and n.value >= 3 * 4000
+    assert lib.tp_csr_workspace_size(-1, 50, ctypes.byref(n)) == 7
+    # workspace too small / misaligned
+    assert lib.tp_csr_build(good, 1000, 50, good, good, vp(0), good, 16, vp(0)) == 7
+    assert lib.tp_csr_build(good, 1000, 50, good, good, vp(0), vp(0x10010), n.value, vp(0)) == 5
+    assert lib.tp_csr_build(good, 10, 0, good, good, vp(0), good, n.value, vp(0)) == 4

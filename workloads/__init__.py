@@ -155,14 +155,16 @@ def make_graph(w: Workload, seed: int = 0):
 
 
 def make_features(rng: np.random.Generator, w: Workload, n_nodes: int, n_edges: int,
-                  dim_x: int, weight_numel: int, n_paths: int, dim_out: int):
+                  dim_x: int, weight_numel: int, n_paths: int, dim_out: int, dtype=np.float64):
     """Draw x [N, dim_x], w [E, weight_numel] and (for backward workloads)
-    grad_out [N, dim_out], all float64, continuing ``rng``."""
-    x = rng.standard_normal((n_nodes, dim_x))
-    wt = rng.standard_normal((n_edges, weight_numel))
+    grad_out [N, dim_out], continuing ``rng``. ``dtype`` float64 (default) or
+    float32; the full-size workloads use float32 draws so the weight stream
+    (up to 1.9e9 values) fits in host memory."""
+    x = rng.standard_normal((n_nodes, dim_x), dtype=dtype)
+    wt = rng.standard_normal((n_edges, weight_numel), dtype=dtype)
     if w.w_scale == "inv_sqrt_paths":
-        wt /= math.sqrt(n_paths)
-    g = rng.standard_normal((n_nodes, dim_out)) if w.backward else None
+        wt *= dtype(1.0 / math.sqrt(n_paths))
+    g = rng.standard_normal((n_nodes, dim_out), dtype=dtype) if w.backward else None
     return x, wt, g
 
 
