@@ -33,12 +33,13 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 TP_OK = 0
 STATUS_NAMES = {0: "TP_OK", 1: "TP_ERR_PARSE", 2: "TP_ERR_UNSUPPORTED", 3: "TP_ERR_UNSORTED", 4: "TP_ERR_INDEX",
-                5: "TP_ERR_ALIGN", 6: "TP_ERR_CUDA", 7: "TP_ERR_ARG", 8: "TP_ERR_TIMEOUT"}
+                5: "TP_ERR_ALIGN", 6: "TP_ERR_CUDA", 7: "TP_ERR_ARG", 8: "TP_ERR_TIMEOUT", 9: "TP_ERR_CAPACITY"}
 TP_F32, TP_BF16_IN_F32_OUT = 0, 1
 TP_IR_MUL, TP_MUL_IR = 0, 1
 TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
 EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
-           "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_conv_forward",
+           "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
+           "tp_csr_build_noalloc_max_edges", "tp_conv_forward",
            "tp_conv_backward", "tp_device_status", "tp_status_string", "tp_abi_version"]
 
 
@@ -68,6 +69,7 @@ _sigs = {
     "tp_spherical_harmonics": [_vp, _vp, _i64, _i32, _vp, _vp],
     "tp_csr_workspace_size": [_i64, _i32, ctypes.POINTER(_sz)],
     "tp_csr_build": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _sz, _vp],
+    "tp_csr_build_noalloc": [_vp, _i64, _i32, _vp, _vp, _vp, _vp],
     "tp_conv_forward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp],
     "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
@@ -79,6 +81,8 @@ _lib.tp_desc_destroy.argtypes = [_vp]
 _lib.tp_desc_destroy.restype = None
 _lib.tp_status_string.argtypes = [ctypes.c_int]
 _lib.tp_status_string.restype = ctypes.c_char_p
+_lib.tp_csr_build_noalloc_max_edges.argtypes = []
+_lib.tp_csr_build_noalloc_max_edges.restype = ctypes.c_int64
 _lib.tp_abi_version.argtypes = []
 _lib.tp_abi_version.restype = ctypes.c_int32
 
@@ -216,6 +220,26 @@ def tp_csr_build(keys, N: int, perm=None, row_ptr=None, keys_sorted=None, worksp
                              _dev_ptr(keys_sorted, "keys_sorted", torch.int32, 1),
                              _dev_ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)),
            "tp_csr_build")
+    return perm, row_ptr, keys_sorted
+
+
+def tp_csr_build_noalloc_max_edges() -> int:
+    return int(_lib.tp_csr_build_noalloc_max_edges())
+
+
+def tp_csr_build_noalloc(keys, N: int, perm, row_ptr, keys_sorted=None, stream=None):
+    """tp_csr_build without any device allocation, for callers that cannot
+    allocate (a stream being captured into a CUDA graph, a plugin's enqueue):
+    the caller passes every output buffer and the library uses its own fixed
+    scratch array (E <= tp_csr_build_noalloc_max_edges()). Calls that overlap
+    on the GPU share that array and race."""
+    torch = _torch()
+    E = keys.shape[0]
+    _check(_lib.tp_csr_build_noalloc(_dev_ptr(keys, "keys", torch.int32, 1), E, N,
+                                     _dev_ptr(perm, "perm", torch.int32, 1),
+                                     _dev_ptr(row_ptr, "row_ptr", torch.int32, 1),
+                                     _dev_ptr(keys_sorted, "keys_sorted", torch.int32, 1), _stream(stream)),
+           "tp_csr_build_noalloc")
     return perm, row_ptr, keys_sorted
 
 

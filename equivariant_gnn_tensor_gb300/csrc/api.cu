@@ -16,6 +16,8 @@ size_t csr_workspace_bytes(int64_t E, int32_t N);
 cudaError_t csr_build_launch(const int32_t *keys, int64_t E, int32_t N, int32_t *perm, int32_t *row_ptr,
                              int32_t *keys_sorted, void *ws, int *status, cudaStream_t stream);
 cudaError_t sh_launch(const float *vec, int64_t E, int normalize, const Tables &T, float *sh, cudaStream_t stream);
+int64_t csr_noalloc_max_edges();
+cudaError_t csr_noalloc_scratch(void **ptr);
 }  // namespace tpc
 
 namespace {
@@ -145,6 +147,25 @@ extern "C" tp_status tp_csr_build(const int32_t *keys, int64_t E, int32_t N, int
         return TP_ERR_CUDA;
     return TP_OK;
 }
+
+extern "C" tp_status tp_csr_build_noalloc(const int32_t *keys, int64_t E, int32_t N, int32_t *perm,
+                                          int32_t *row_ptr, int32_t *keys_sorted, void *stream) {
+    if (E < 0 || N < 0 || !row_ptr) return TP_ERR_ARG;
+    if (E > csr_noalloc_max_edges()) return TP_ERR_CAPACITY;
+    if (E > 0 && (!keys || !perm)) return TP_ERR_ARG;
+    if (E > 0 && N == 0) return TP_ERR_INDEX;
+    DevInfo dev;
+    tp_status st = dev_info(dev);
+    if (st != TP_OK) return st;
+    void *scratch = nullptr;
+    if (csr_noalloc_scratch(&scratch) != cudaSuccess) return TP_ERR_CUDA;
+    if (csr_build_launch(keys, E, N, perm, row_ptr, keys_sorted, scratch, dev.status,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TP_ERR_CUDA;
+    return TP_OK;
+}
+
+extern "C" int64_t tp_csr_build_noalloc_max_edges(void) { return csr_noalloc_max_edges(); }
 
 extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const void *x, const float *sh, const void *w,
                                      const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
@@ -286,6 +307,7 @@ extern "C" const char *tp_status_string(tp_status s) {
         case TP_ERR_CUDA: return "CUDA runtime error";
         case TP_ERR_ARG: return "invalid argument";
         case TP_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case TP_ERR_CAPACITY: return "size exceeds the fixed scratch capacity of this entry point";
     }
     return "unknown status";
 }

@@ -15,6 +15,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+
 #include "../../include/tpconv.h"
 #include "common.cuh"
 
@@ -193,6 +196,41 @@ cudaError_t csr_build_launch(const int32_t *keys, int64_t E, int32_t N, int32_t 
     }
     row_ptr_kernel<<<(int)((N + 1 + 255) / 256), 256, 0, stream>>>(fin_k, E, N, row_ptr);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the sort's scratch lives in this fixed device array
+// instead of caller memory. Sized for kNoAllocMaxEdges keys (any N): three
+// int32 arrays of that length plus the per-tile digit counts.
+constexpr int64_t kNoAllocMaxEdges = int64_t(1) << 18;
+constexpr size_t kNoAllocBytes =
+    (sizeof(int32_t) * kNoAllocMaxEdges + 255) / 256 * 256 * 3 +
+    (sizeof(int32_t) * 256 * ((kNoAllocMaxEdges + kTile - 1) / kTile) + 255) / 256 * 256;
+static __device__ __align__(256) unsigned char g_csr_scratch[kNoAllocBytes];
+
+int64_t csr_noalloc_max_edges() { return kNoAllocMaxEdges; }
+
+// Device address of g_csr_scratch on the current device, looked up once per
+// device (the name is only a host-side stand-in for the symbol).
+cudaError_t csr_noalloc_scratch(void **ptr) {
+    static std::mutex mu;
+    static std::map<int, void *> addr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = addr.find(dev);
+    if (it != addr.end()) {
+        *ptr = it->second;
+        return cudaSuccess;
+    }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_csr_scratch);
+    if (e != cudaSuccess) return e;
+    if (csr_workspace_bytes(kNoAllocMaxEdges, 1) > kNoAllocBytes) return cudaErrorInvalidValue;
+    addr[dev] = p;
+    *ptr = p;
+    return cudaSuccess;
 }
 
 }  // namespace tpc

@@ -71,7 +71,8 @@ typedef enum {
     TP_ERR_ALIGN = 5,       /* a pointer or row size breaks the 16-byte rule */
     TP_ERR_CUDA = 6,        /* a CUDA runtime call failed */
     TP_ERR_ARG = 7,         /* null pointer, negative size or bad enum */
-    TP_ERR_TIMEOUT = 8      /* a device pipeline wait gave up (device status bit) */
+    TP_ERR_TIMEOUT = 8,     /* a device pipeline wait gave up (device status bit) */
+    TP_ERR_CAPACITY = 9     /* size exceeds a fixed capacity (tp_csr_build_noalloc) */
 } tp_status;
 
 typedef enum { TP_IR_MUL = 0, TP_MUL_IR = 1 } tp_layout;
@@ -149,6 +150,26 @@ TPCONV_API tp_status tp_csr_workspace_size(int64_t E, int32_t N, size_t *bytes);
  * unspecified but every write stays inside the output arrays. */
 TPCONV_API tp_status tp_csr_build(const int32_t *keys, int64_t E, int32_t N, int32_t *perm, int32_t *row_ptr,
                        int32_t *keys_sorted, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Allocation-free tp_csr_build. The pages have no counterpart: this entry
+ * point exists for callers that must not allocate device memory at all, for
+ * example a plugin's enqueue function or code running while a stream is being
+ * captured into a CUDA graph (cudaMalloc is not allowed there, and elsewhere it
+ * may synchronise the device), or a program whose device memory is entirely
+ * owned by another allocator. Results are identical to tp_csr_build.
+ * The sort's scratch is a fixed array inside the library (about 3.3 MB, held on
+ * every GPU that loads the library until the process exits); the caller still
+ * passes keys and the outputs. E may be at most
+ * tp_csr_build_noalloc_max_edges() (262144); larger E returns TP_ERR_CAPACITY
+ * without launching anything. The first call on each device looks up the
+ * array's device address (a one-time set-up, no allocation); make that first
+ * call before capturing a stream. All calls share the one array, so calls that
+ * overlap on the GPU (different streams, or different host threads) race and
+ * must be serialised by the caller. Nothing in the array needs to start at
+ * zero: every call overwrites what it reads. */
+TPCONV_API tp_status tp_csr_build_noalloc(const int32_t *keys, int64_t E, int32_t N, int32_t *perm,
+                                          int32_t *row_ptr, int32_t *keys_sorted, void *stream);
+TPCONV_API int64_t tp_csr_build_noalloc_max_edges(void);
 
 /* Forward pass (the hot path). Edges must be in destination-sorted order with
  * row_ptr[N_dst+1] from tp_csr_build (edge range of destination d is
