@@ -39,7 +39,7 @@ TP_IR_MUL, TP_MUL_IR = 0, 1
 TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
 EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
            "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
-           "tp_csr_build_noalloc_max_edges", "tp_conv_forward",
+           "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
            "tp_conv_backward", "tp_device_status", "tp_status_string", "tp_abi_version"]
 
 
@@ -70,7 +70,8 @@ _sigs = {
     "tp_csr_workspace_size": [_i64, _i32, ctypes.POINTER(_sz)],
     "tp_csr_build": [_vp, _i64, _i32, _vp, _vp, _vp, _vp, _sz, _vp],
     "tp_csr_build_noalloc": [_vp, _i64, _i32, _vp, _vp, _vp, _vp],
-    "tp_conv_forward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp],
+    "tp_conv_forward_workspace_size": [_vp, ctypes.c_int, _i32, _i64, ctypes.POINTER(_sz)],
+    "tp_conv_forward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _sz, _vp],
     "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
 }
@@ -243,22 +244,42 @@ def tp_csr_build_noalloc(keys, N: int, perm, row_ptr, keys_sorted=None, stream=N
     return perm, row_ptr, keys_sorted
 
 
-def tp_conv_forward(desc: Descriptor, x, sh, w, src, row_ptr, n_dst: int, out=None, stream=None):
-    """out[n_dst, dim_out] float32 for destination-sorted edges. x and w are both
-    float32 (TP_F32) or both bfloat16 (TP_BF16_IN_F32_OUT)."""
+def _fwd_dtype(x, w):
     torch = _torch()
     if x.dtype != w.dtype:
         raise TypeError("x and w must have the same dtype")
     dtype = {torch.float32: TP_F32, torch.bfloat16: TP_BF16_IN_F32_OUT}.get(x.dtype)
     if dtype is None:
         raise TypeError(f"unsupported dtype {x.dtype}")
+    return dtype
+
+
+def tp_conv_forward_workspace_size(desc: Descriptor, dtype: int, n_dst: int, E: int) -> int:
+    n = _sz()
+    _check(_lib.tp_conv_forward_workspace_size(desc.handle, dtype, n_dst, E, ctypes.byref(n)),
+           "tp_conv_forward_workspace_size")
+    return int(n.value)
+
+
+def tp_conv_forward(desc: Descriptor, x, sh, w, src, row_ptr, n_dst: int, out=None, workspace="auto", stream=None):
+    """out[n_dst, dim_out] float32 for destination-sorted edges. x and w are both
+    float32 (TP_F32) or both bfloat16 (TP_BF16_IN_F32_OUT). `workspace`: a
+    uint8 CUDA tensor of tp_conv_forward_workspace_size bytes, "auto" to
+    allocate one here, or None for the generic (workspace-free) kernel."""
+    torch = _torch()
+    dtype = _fwd_dtype(x, w)
     E = src.shape[0]
     if out is None:
         out = torch.empty((n_dst, desc.dim_out), dtype=torch.float32, device=x.device)
+    if isinstance(workspace, str):
+        nb = tp_conv_forward_workspace_size(desc, dtype, n_dst, E)
+        workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_n = workspace.numel() if workspace is not None else 0
     _check(_lib.tp_conv_forward(desc.handle, dtype, _dev_ptr(x, "x", None, 2), _dev_ptr(sh, "sh", torch.float32, 2),
                                 _dev_ptr(w, "w", None, 2), _dev_ptr(src, "src", torch.int32, 1),
                                 _dev_ptr(row_ptr, "row_ptr", torch.int32, 1), x.shape[0], n_dst, E,
-                                _dev_ptr(out, "out", torch.float32, 2), _stream(stream)),
+                                _dev_ptr(out, "out", torch.float32, 2), ws_ptr, ws_n, _stream(stream)),
            "tp_conv_forward")
     return out
 

@@ -18,6 +18,11 @@ cudaError_t csr_build_launch(const int32_t *keys, int64_t E, int32_t N, int32_t 
 cudaError_t sh_launch(const float *vec, int64_t E, int normalize, const Tables &T, float *sh, cudaStream_t stream);
 int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
+size_t team_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin);
+cudaError_t team_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
+                         const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
+                         float *out, void *ws, size_t ws_bytes, int sms, int smem_optin, int *status,
+                         cudaStream_t stream);
 }  // namespace tpc
 
 namespace {
@@ -167,9 +172,20 @@ extern "C" tp_status tp_csr_build_noalloc(const int32_t *keys, int64_t E, int32_
 
 extern "C" int64_t tp_csr_build_noalloc_max_edges(void) { return csr_noalloc_max_edges(); }
 
+extern "C" tp_status tp_conv_forward_workspace_size(const tp_desc *desc, tp_dtype dtype, int32_t N_dst, int64_t E,
+                                                    size_t *bytes) {
+    if (!desc || !bytes || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
+    DevInfo dev;
+    tp_status st = dev_info(dev);
+    if (st != TP_OK) return st;
+    *bytes = team_workspace_bytes(desc, dtype, E, dev.sms, dev.smem_optin);
+    return TP_OK;
+}
+
 extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const void *x, const float *sh, const void *w,
                                      const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
-                                     int64_t E, float *out, void *stream) {
+                                     int64_t E, float *out, void *workspace, size_t workspace_bytes, void *stream) {
     if (!desc || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
     if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
     if (N_dst == 0) return TP_OK;
@@ -182,6 +198,18 @@ extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
     if ((f_bytes & 15) || (w_bytes & 15)) return TP_ERR_ALIGN;
     if (!aligned16(out) || (E > 0 && (!aligned16(x) || !aligned16(w) || !aligned4(sh) || !aligned4(src))))
         return TP_ERR_ALIGN;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP_ERR_ALIGN;
+    {
+        DevInfo dev;
+        tp_status st = dev_info(dev);
+        if (st != TP_OK) return st;
+        const cudaError_t e = team_forward(desc, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, workspace,
+                                           workspace_bytes, dev.sms, dev.smem_optin, dev.status,
+                                           static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) return TP_OK;
+        if (e != cudaErrorNotSupported) return TP_ERR_CUDA;
+        (void)cudaGetLastError();
+    }
     Shape shp;
     if (!pick_shape(desc->lmax_in, desc->lmax_out, shp)) return TP_ERR_UNSUPPORTED;
     const int cpt = pick_cpt(T.mul);

@@ -22,6 +22,7 @@
 #include <vector>
 
 #include "../../include/tpconv.h"
+#include "program.h"
 #include "tables.h"
 
 namespace {
@@ -165,6 +166,84 @@ void real_cg(int l1, int l2, int l3, double *C) {
     for (size_t q = 0; q < T.size(); ++q) C[q] *= sign;
 }
 
+// Match the descriptor against the compiled path programs (program.h) and
+// build the program-layout recipe for the first one that fits.
+void plan_team(tp_desc *d) {
+    using namespace tpc;
+    TeamPlan &TP = d->team;
+    TP.valid = 0;
+    for (int si = 0; si < kNumProgShapes; ++si) {
+        const ProgShape sh = kProgShapes[si];
+        const Program P = make_natural_program(sh.li, sh.lsh, sh.lo);
+        if (P.n != d->n_paths || P.n > 32) continue;
+        bool ok = true;
+        for (int c = 0; c < d->n_out; ++c) ok = ok && d->out_l[c] <= sh.lo;
+        for (int a = 0; a < d->n_in; ++a) ok = ok && d->in_l[a] <= sh.li;
+        if (!ok) continue;
+        int map[kProgMaxPaths];
+        bool used[kMaxPaths] = {};
+        for (int t = 0; t < P.n && ok; ++t) {
+            map[t] = -1;
+            for (int p = 0; p < d->n_paths; ++p) {
+                if (used[p]) continue;
+                if (d->in_l[d->path_a[p]] == P.p[t].la && d->sh_l[d->path_b[p]] == P.p[t].lb &&
+                    d->out_l[d->path_c[p]] == P.p[t].lc) {
+                    map[t] = p;
+                    used[p] = true;
+                    break;
+                }
+            }
+            ok = map[t] >= 0;
+        }
+        if (!ok) continue;
+        // every nonzero C[i,j,k] must have (i,k) inside the pattern
+        for (int t = 0; t < P.n && ok; ++t) {
+            const int p = map[t];
+            const int la = P.p[t].la, lb = P.p[t].lb, lc = P.p[t].lc;
+            const int n2 = 2 * lb + 1, n3 = 2 * lc + 1;
+            for (int i = 0; i < 2 * la + 1 && ok; ++i)
+                for (int k = 0; k < n3 && ok; ++k) {
+                    bool nz = false;
+                    for (int j = 0; j < n2; ++j) nz = nz || d->cg[p][(i * n2 + j) * n3 + k] != 0.0;
+                    if (nz && !m_entry_possible(la, lb, lc, i, k)) ok = false;
+                }
+        }
+        if (!ok || P.R > kMaxM) continue;
+        int nnz = 0;
+        for (int r = 0; r < P.R; ++r) {
+            TP.ej[r] = 0;
+            TP.ec[r][0] = TP.ec[r][1] = 0.f;
+        }
+        for (int t = 0; t < P.n && ok; ++t) {
+            const int p = map[t];
+            const int lb = P.p[t].lb, lc = P.p[t].lc;
+            const int n2 = 2 * lb + 1, n3 = 2 * lc + 1;
+            TP.wofs[t] = (int16_t)(p * d->tab.mul);
+            for (int q = 0; q < P.nz[t]; ++q) {
+                const int r = P.moff[t] + q;
+                const int i = P.ik[t][q] >> 3, k = P.ik[t][q] & 7;
+                int terms = 0;
+                for (int j = 0; j < n2; ++j) {
+                    const double c = d->cg[p][(i * n2 + j) * n3 + k];
+                    if (c == 0.0) continue;
+                    if (terms == 2) { ok = false; break; }
+                    const uint32_t jg = (uint32_t)(d->sh_off[d->path_b[p]] + j);
+                    TP.ej[r] |= terms == 0 ? jg : (jg << 16);
+                    TP.ec[r][terms] = (float)c;
+                    ++terms;
+                    ++nnz;
+                }
+            }
+        }
+        if (!ok) continue;
+        TP.R = P.R;
+        TP.nnz = nnz;
+        TP.shape = si;
+        TP.valid = 1;
+        return;
+    }
+}
+
 void free_desc(tp_desc *d) {
     if (!d) return;
     for (int p = 0; p < d->n_paths; ++p) std::free(d->cg[p]);
@@ -294,6 +373,7 @@ extern "C" tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh
         for (auto &e : col[j]) { T.tr_r[t] = (uint16_t)e.first; T.tr_c[t] = e.second; ++t; }
     }
     T.tr_ptr[dim_sh] = (uint16_t)t;
+    plan_team(d);
     *out = d;
     return TP_OK;
 }

@@ -41,6 +41,19 @@ struct Tables {
     float tr_c[kMaxTerms];
 };
 
+// Runtime tables for a compile-time path program (program.h): valid when the
+// descriptor's paths are exactly the program's and every nonzero
+// Clebsch-Gordan entry lies inside the program's M pattern.
+struct TeamPlan {
+    int32_t valid;
+    int32_t shape;   // index into kProgShapes
+    int32_t R, nnz;
+    int16_t wofs[32];  // weight-row offset (elements) of program path t
+    // M entry r (program layout) = ec[r][0] * sh[ej[r] & 0xffff] + ec[r][1] * sh[ej[r] >> 16]
+    uint32_t ej[kMaxM];
+    float ec[kMaxM][2];
+};
+
 }  // namespace tpc
 
 struct tp_desc {
@@ -55,4 +68,5 @@ struct tp_desc {
     int path_a[tpc::kMaxPaths], path_b[tpc::kMaxPaths], path_c[tpc::kMaxPaths];
     double *cg[tpc::kMaxPaths];  // dense [2la+1][2lb+1][2lc+1]
     tpc::Tables tab;
+    tpc::TeamPlan team;
 };

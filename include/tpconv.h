@@ -86,6 +86,7 @@ typedef enum {
 #define TP_DEV_ERR_INDEX 0x1   /* src/dst/key outside [0, N) - the edge was skipped */
 #define TP_DEV_ERR_TIMEOUT 0x2 /* an mbarrier wait exceeded its iteration limit */
 #define TP_DEV_ERR_SEGMENT 0x4 /* row pointers not non-decreasing or outside [0, E] */
+#define TP_DEV_ERR_INTERNAL 0x8 /* a kernel's own consistency check failed (a library bug); the access was skipped */
 
 typedef struct tp_desc tp_desc;
 
@@ -179,14 +180,23 @@ TPCONV_API int64_t tp_csr_build_noalloc_max_edges(void);
  *   w:   device [E][weight_numel], same type as x;
  *   src: device int32 [E], in [0, N_src);
  *   out: device float32 [N_dst][dim_out], fully overwritten (zero rows for
- *        destinations without edges).
+ *        destinations without edges);
+ *   workspace: device memory of tp_conv_forward_workspace_size() bytes
+ *        (256-byte aligned), or NULL. It holds the partial rows of destinations
+ *        that straddle the kernel's exact, edge-balanced split of the edge list;
+ *        with NULL (or too small) the library uses its generic kernel, which
+ *        needs none but splits work per destination.
  * x, w and out must be 16-byte aligned; dim_x*sizeof(x) and
  * weight_numel*sizeof(w) must be multiples of 16 (they are whenever mul % 8
  * == 0). Out-of-range src entries are skipped and set TP_DEV_ERR_INDEX.
- * Summation order is fixed: results are bitwise reproducible run to run. */
+ * Summation order is fixed: results are bitwise reproducible run to run on
+ * one device (the split depends on the device's SM count). */
+TPCONV_API tp_status tp_conv_forward_workspace_size(const tp_desc *desc, tp_dtype dtype, int32_t N_dst, int64_t E,
+                                                    size_t *bytes);
 TPCONV_API tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const void *x, const float *sh,
-                          const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src,
-                          int32_t N_dst, int64_t E, float *out, void *stream);
+                                     const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src,
+                                     int32_t N_dst, int64_t E, float *out, void *workspace,
+                                     size_t workspace_bytes, void *stream);
 
 /* Backward pass of tp_conv_forward (float32), the exact gradients of
  * <grad_out, out> with respect to x, w and sh:

@@ -14,10 +14,11 @@ from workloads import WORKLOADS, make_features, make_graph
 pytestmark = pytest.mark.gpu
 
 
-def run(tpc, prob, dtype=torch.float32):
+def run(tpc, prob, dtype=torch.float32, workspace="auto"):
     desc = tpc.tp_desc_create(*prob["irreps"])
     g = gpu_sorted_inputs(tpc, prob, dtype)
-    out = tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], g["row_ptr"], prob["n_dst"])
+    out = tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], g["row_ptr"], prob["n_dst"],
+                              workspace=workspace)
     torch.cuda.synchronize()
     return out, desc, g
 
@@ -35,19 +36,24 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["split", "generic"])
 @pytest.mark.parametrize("irr", SHAPES, ids=lambda c: "|".join(c))
-def test_forward_matches_oracle(tpc, irr):
+def test_forward_matches_oracle(tpc, irr, workspace):
+    """With a workspace, shapes that have a compiled path program run the
+    edge-balanced kernel (destinations cut across CTAs are merged from
+    partials); without one, or for other shapes, the per-destination kernel."""
     prob = make_problem(*irr, n_src=300, n_dst=257, E=5000, seed=1)
-    out, _, _ = run(tpc, prob)
+    out, _, _ = run(tpc, prob, workspace=workspace)
     ref = oracle_forward(prob)
     assert err(out, ref) <= FP32_TOL
     assert tpc.tp_device_status(reset=True) == 0
 
 
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["split", "generic"])
 @pytest.mark.parametrize("irr", SHAPES[:3], ids=lambda c: "|".join(c))
-def test_forward_bf16_inputs(tpc, irr):
+def test_forward_bf16_inputs(tpc, irr, workspace):
     prob = make_problem(*irr, n_src=200, n_dst=190, E=3000, seed=2)
-    out, _, _ = run(tpc, prob, torch.bfloat16)
+    out, _, _ = run(tpc, prob, torch.bfloat16, workspace=workspace)
     ref = oracle_forward(prob, torch.bfloat16)
     e = err(out, ref)
     assert e <= BF16_TOL
@@ -66,14 +72,16 @@ def test_tiny_workload(tpc):
     assert err(out, oracle_forward(prob)) <= FP32_TOL
 
 
-def test_degree_extremes_and_empty_rows(tpc):
-    """One destination with 1000 edges (many chunks), many with none, a ragged mix."""
+@pytest.mark.parametrize("workspace", ["auto", None], ids=["split", "generic"])
+def test_degree_extremes_and_empty_rows(tpc, workspace):
+    """One destination with 1000 edges (many chunks, cut across several CTAs
+    by the edge-balanced split), many with none, a ragged mix."""
     rng = np.random.default_rng(5)
     n_dst = 700
     dst = np.concatenate([np.full(1000, 3), rng.integers(0, n_dst // 2, 3000) * 2, [n_dst - 1]])
     rng.shuffle(dst)
     prob = make_problem(*SHAPES[1], n_src=50, n_dst=n_dst, E=len(dst), seed=6, dst=dst)
-    out, _, _ = run(tpc, prob)
+    out, _, _ = run(tpc, prob, workspace=workspace)
     ref = oracle_forward(prob)
     # destination 3 sums 1000 edges: judge every row against its own RMS (the
     # whole-tensor RMS, diluted by empty rows, understates its magnitude)
@@ -106,6 +114,30 @@ def test_bipartite_sources(tpc):
     prob = make_problem(*SHAPES[3], n_src=3, n_dst=900, E=3000, seed=10)
     out, _, _ = run(tpc, prob)
     assert err(out, oracle_forward(prob)) <= FP32_TOL
+
+
+@pytest.mark.parametrize("pipelined", ["0", "1"], ids=["ring", "cta-pipeline"])
+@pytest.mark.parametrize("irr,dtype", [(SHAPES[0], torch.float32), (SHAPES[1], torch.float32),
+                                       (SHAPES[2], torch.bfloat16), (SHAPES[3], torch.float32)],
+                         ids=["tiny", "medium", "large-bf16", "lesson"])
+def test_both_split_kernels(tpc, monkeypatch, irr, dtype, pipelined):
+    """Both edge-balanced kernels (the per-warp cp.async ring and the CTA
+    pipeline with a TMA producer warp) against the oracle, whichever the
+    library would pick by default."""
+    monkeypatch.setenv("TPCONV_FWD_PIPELINED", pipelined)
+    prob = make_problem(*irr, n_src=400, n_dst=333, E=9000, seed=14)
+    out, _, _ = run(tpc, prob, dtype)
+    tol = FP32_TOL
+    assert err(out, oracle_forward(prob, dtype)) <= tol
+    assert tpc.tp_device_status(reset=True) == 0
+
+
+def test_split_kernel_is_used_for_program_shapes(tpc):
+    for irr in SHAPES[:4]:
+        desc = tpc.tp_desc_create(*irr)
+        assert tpc.tp_conv_forward_workspace_size(desc, tpc.TP_F32, 1000, 100000) > 0, irr
+    desc = tpc.tp_desc_create(*SHAPES[4])   # SO(3): no compiled program
+    assert tpc.tp_conv_forward_workspace_size(desc, tpc.TP_F32, 1000, 100000) == 0
 
 
 def test_deterministic(tpc):

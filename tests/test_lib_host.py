@@ -82,17 +82,17 @@ def test_argument_errors_need_no_gpu(tpc):
     vp = ctypes.c_void_p
     good, odd = vp(0x10000), vp(0x10004)
     # null out / row_ptr
-    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, vp(0), 4, 4, 10, good, vp(0)) == 7
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, vp(0), 4, 4, 10, good, vp(0), 0, vp(0)) == 7
     # misaligned x
-    assert lib.tp_conv_forward(d.handle, 0, odd, good, good, good, good, 4, 4, 10, good, vp(0)) == 5
+    assert lib.tp_conv_forward(d.handle, 0, odd, good, good, good, good, 4, 4, 10, good, vp(0), 0, vp(0)) == 5
     # negative sizes, bad dtype, E >= 2^31
-    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, -1, 4, 10, good, vp(0)) == 7
-    assert lib.tp_conv_forward(d.handle, 5, good, good, good, good, good, 4, 4, 10, good, vp(0)) == 7
-    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, 4, 4, 1 << 31, good, vp(0)) == 7
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, -1, 4, 10, good, vp(0), 0, vp(0)) == 7
+    assert lib.tp_conv_forward(d.handle, 5, good, good, good, good, good, 4, 4, 10, good, vp(0), 0, vp(0)) == 7
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, 4, 4, 1 << 31, good, vp(0), 0, vp(0)) == 7
     # edges but no source nodes
-    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, 0, 4, 10, good, vp(0)) == 4
+    assert lib.tp_conv_forward(d.handle, 0, good, good, good, good, good, 0, 4, 10, good, vp(0), 0, vp(0)) == 4
     # no destinations: nothing to do
-    assert lib.tp_conv_forward(d.handle, 0, vp(0), vp(0), vp(0), vp(0), vp(0), 0, 0, 0, vp(0), vp(0)) == 0
+    assert lib.tp_conv_forward(d.handle, 0, vp(0), vp(0), vp(0), vp(0), vp(0), 0, 0, 0, vp(0), vp(0), 0, vp(0)) == 0
     n = ctypes.c_size_t()
     assert lib.tp_csr_workspace_size(1000, 50, ctypes.byref(n)) == 0 and n.value >= 3 * 4000
     assert lib.tp_csr_workspace_size(-1, 50, ctypes.byref(n)) == 7
