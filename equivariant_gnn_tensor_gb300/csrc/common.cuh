@@ -10,9 +10,12 @@
 
 namespace tpc {
 
-// An mbarrier wait gives up after this long (nanoseconds of %globaltimer), so
-// a lost copy turns into a status bit instead of a hung GPU.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// An mbarrier wait gives up after this many probes (each followed, after the
+// first few, by a ~20 ns sleep: about a second in all), so a lost copy turns
+// into a status bit instead of a hung GPU. Probes are counted rather than
+// timed: reading a clock in the wait loop sits on the critical path of every
+// handoff.
+constexpr uint32_t kWaitProbes = 1u << 25;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -76,15 +79,13 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Bounded wait: true when the phase completed, false after kWaitLimitNs.
+// Bounded wait: true when the phase completed, false after kWaitProbes probes.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+    for (uint32_t it = 0; it < kWaitProbes; ++it) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (it >= 32) __nanosleep(20);
     }
+    return false;
 }
 
 // Order this thread's earlier generic-proxy shared-memory accesses before

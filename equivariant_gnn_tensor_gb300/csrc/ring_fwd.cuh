@@ -1,0 +1,539 @@
+// Forward kernel for irreps shapes with a compile-time path program
+// (program.h) in the natural layout (input blocks l = 0..LI, output blocks
+// l = 0..LO, mul = 32*CPT channels each, paths in program order): every warp
+// warp is an independent pipeline that copies its own edges into a private
+// S-stage shared-memory ring with 1-D bulk (TMA) copies and consumes them
+// itself. There is no producer warp and no barrier between warps; the only
+// synchronisation is the warp's own mbarrier per stage.
+//
+// Work split: the destination-sorted edge list is cut into `n_pieces` exact,
+// contiguous, equal pieces; piece p belongs to warp p % n_warps, so with
+// several pieces per warp ("rounds") the whole grid sweeps the edge list front
+// to back together, which keeps the gathered source rows of neighbouring
+// destinations in L2 at the same time.
+//
+// Per warp:
+//   issue:   chunks of up to `eps` consecutive edges of its pieces, in order;
+//            one bulk copy for the chunk's weight rows, one for the 16-byte
+//            aligned span around its harmonic rows, one per edge for the
+//            gathered source row x[src[e]]. The source indices of the next two
+//            chunks are loaded ahead into registers.
+//   consume: wait for the chunk's stage, build the per-edge matrices
+//            M_p[i][k] = sum_j C_p[i,j,k] sh[j] (program layout, at most two
+//            terms per entry) into a warp-private buffer, then run every path as
+//            straight-line code into the destination row held in registers
+//            (lane = CPT consecutive channels, so one warp covers all channels;
+//            with PK two channels share one packed fma.rn.f32x2, whose halves
+//            round exactly like two fmaf: half the issue slots, but a longer
+//            dependent latency), refill the stage with the chunk S ahead.
+//   store:   when a destination ends its row is written once; a destination cut
+//            by a piece boundary is written as a head/tail partial that
+//            carry_fixup_kernel adds in piece order. No atomics: results are
+//            bitwise reproducible for a given launch geometry.
+#pragma once
+#include "team_fwd.cuh"
+
+namespace tpc {
+
+constexpr int kRingMaxWarps = 8;
+constexpr int kRingMaxPiecesPerWarp = 16;
+
+struct RingParams {
+    int32_t S, eps;                      // stages per warp, edges per chunk (<= 32)
+    int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0, source rows, harmonic span
+    int32_t m_off, meta_off, bar_off, warp_bytes;  // warp region: stages, M, chunk meta, barriers
+    int32_t tab_bytes;                   // block-shared M recipe table at the start of shared memory
+    int32_t x_lsu;                       // 1: gathered rows by 16-byte cp.async from all lanes, 0: one bulk copy each
+    uint32_t ej[kMaxM];
+    float ec[kMaxM][2];
+    const void *x;
+    const float *sh;
+    const void *w;
+    const int32_t *src;
+    const int32_t *row_ptr;
+    float *out;
+    float *carry;        // [2*n_pieces][dim_out]
+    int32_t *carry_dst;  // [2*n_pieces]
+    int *status;
+    int32_t n_src, n_dst, n_warps, n_pieces;
+    int64_t E;
+};
+
+// Smallest d in [0, N] with rp[d] >= target (N+1 if none): one lane's binary search.
+__device__ __forceinline__ int lane_first_geq(const int32_t *rp, int N, int64_t target) {
+    int lo = 0, hi = N + 1;
+    while (lo < hi) {
+        const int mid = lo + ((hi - lo) >> 1);
+        if ((int64_t)rp[mid] >= target) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+// ---- lane values: CPT channels as floats (CPT = 1) or packed pairs (CPT >= 2) ----
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ void vfma(float &d, float a, float b) { d = fmaf(a, b, d); }
+__device__ __forceinline__ float vmul(float a, float b) { return a * b; }
+__device__ __forceinline__ void vfma(f32x2 &d, f32x2 a, f32x2 b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ f32x2 vmul(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
+template <int CPT, bool PK>
+struct LaneVec {
+    static constexpr bool kPair = PK && CPT >= 2;
+    static constexpr int NV = kPair ? CPT / 2 : CPT;
+    using V = typename std::conditional<kPair, f32x2, float>::type;
+};
+
+// CPT consecutive channels starting at p (shared memory), as lane values.
+template <int CPT, bool PK>
+__device__ __forceinline__ void load_lane(const float *p, typename LaneVec<CPT, PK>::V (&v)[LaneVec<CPT, PK>::NV]) {
+    if constexpr (LaneVec<CPT, PK>::kPair) {
+        if constexpr (CPT == 4) {
+            const ulonglong2 t = *reinterpret_cast<const ulonglong2 *>(p);
+            v[0] = t.x;
+            v[1] = t.y;
+        } else {
+            v[0] = *reinterpret_cast<const f32x2 *>(p);
+        }
+    } else {
+        load_vec<CPT>(p, v);
+    }
+}
+template <int CPT, bool PK>
+__device__ __forceinline__ void load_lane(const __nv_bfloat16 *p,
+                                          typename LaneVec<CPT, PK>::V (&v)[LaneVec<CPT, PK>::NV]) {
+    if constexpr (LaneVec<CPT, PK>::kPair) {
+        if constexpr (CPT == 4) {
+            const uint2 t = *reinterpret_cast<const uint2 *>(p);
+            v[0] = pack2(bf16lo(t.x), bf16hi(t.x));
+            v[1] = pack2(bf16lo(t.y), bf16hi(t.y));
+        } else {
+            const uint32_t t = *reinterpret_cast<const uint32_t *>(p);
+            v[0] = pack2(bf16lo(t), bf16hi(t));
+        }
+    } else {
+        load_vec<CPT>(p, v);
+    }
+}
+
+// Does entry q of path T write an accumulator row k that no earlier entry wrote?
+template <int LI, int LSH, int LO>
+constexpr bool first_of_k(int T, int q) {
+    constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
+    for (int q2 = 0; q2 < q; ++q2)
+        if ((P.ik[T][q2] & 7) == (P.ik[T][q] & 7)) return false;
+    return true;
+}
+template <int LI, int LSH, int LO>
+constexpr bool has_k(int T, int k) {
+    constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
+    for (int q = 0; q < P.nz[T]; ++q)
+        if ((P.ik[T][q] & 7) == k) return true;
+    return false;
+}
+template <int LI, int LSH, int LO>
+constexpr bool has_i(int T, int i) {
+    constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
+    for (int q = 0; q < P.nz[T]; ++q)
+        if ((P.ik[T][q] >> 3) == i) return true;
+    return false;
+}
+
+// Emission order of the entries of path T: by rank among the entries of the
+// same accumulator row k, then by position. Consecutive FMAs then mostly
+// target different rows, while each row still receives its terms in program
+// order (so the sums are the same as in plain order).
+template <int LI, int LSH, int LO>
+constexpr int entry_at(int T, int pos) {
+    constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
+    int seen = 0;
+    for (int rank = 0; rank < kProgMaxNz; ++rank)
+        for (int q = 0; q < P.nz[T]; ++q) {
+            int r = 0;
+            for (int q2 = 0; q2 < q; ++q2) r += (P.ik[T][q2] & 7) == (P.ik[T][q] & 7);
+            if (r != rank) continue;
+            if (seen == pos) return q;
+            ++seen;
+        }
+    return -1;
+}
+
+// One program path for one edge: acc[lc-block row k] += w_T * sum_i M_T[i][k] x[la-block row i].
+// wl: this lane's channels of the edge's weight row; Mq: the edge's M (entries
+// duplicated into pairs when packed).
+template <int LI, int LSH, int LO, int T, int CPT, bool PK, typename FT>
+__device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[rows_upto(LO)][LaneVec<CPT, PK>::NV],
+                                          const typename LaneVec<CPT, PK>::V (&xr)[rows_upto(LI)][LaneVec<CPT, PK>::NV],
+                                          const FT *wl, const float *Mq) {
+    using LV = LaneVec<CPT, PK>;
+    constexpr int MUL = 32 * CPT;
+    using V = typename LV::V;
+    constexpr int NV = LV::NV;
+    constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
+    constexpr int LA = P.p[T].la, LC = P.p[T].lc;
+    constexpr int NA = 2 * LA + 1, NC = 2 * LC + 1, NZ = P.nz[T], MO = P.moff[T];
+    V wv[NV];
+    load_lane<CPT, PK>(wl + T * MUL, wv);
+    // M entries of this path: 4 per 16-byte load (singles) or 2 (pairs)
+    constexpr int PER = LV::kPair ? 2 : 4;
+    constexpr int NL = (NZ + PER - 1) / PER;
+    V m[NL * PER];
+    if constexpr (LV::kPair) {
+        const ulonglong2 *M2 = reinterpret_cast<const ulonglong2 *>(Mq + 2 * MO);
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+            const ulonglong2 t = M2[q];
+            m[2 * q] = t.x;
+            m[2 * q + 1] = t.y;
+        }
+    } else {
+        const float4 *M4 = reinterpret_cast<const float4 *>(Mq + MO);
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+            const float4 t = M4[q];
+            m[4 * q] = t.x;
+            m[4 * q + 1] = t.y;
+            m[4 * q + 2] = t.z;
+            m[4 * q + 3] = t.w;
+        }
+    }
+    if constexpr (NA <= NC) {
+        V wx[NA][NV];
+        static_for<NA>([&](auto ic) {
+            constexpr int i = decltype(ic)::value;
+            if constexpr (has_i<LI, LSH, LO>(T, i)) {
+#pragma unroll
+                for (int c = 0; c < NV; ++c) wx[i][c] = vmul(wv[c], xr[LA * LA + i][c]);
+            }
+        });
+        static_for<NZ>([&](auto pc) {
+            constexpr int q = entry_at<LI, LSH, LO>(T, decltype(pc)::value);
+            constexpr int i = P.ik[T][q] >> 3, k = P.ik[T][q] & 7;
+#pragma unroll
+            for (int c = 0; c < NV; ++c) vfma(acc[LC * LC + k][c], m[q], wx[i][c]);
+        });
+    } else {
+        V tk[NC][NV];
+        static_for<NZ>([&](auto pc) {
+            constexpr int q = entry_at<LI, LSH, LO>(T, decltype(pc)::value);
+            constexpr int i = P.ik[T][q] >> 3, k = P.ik[T][q] & 7;
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                if constexpr (first_of_k<LI, LSH, LO>(T, q)) tk[k][c] = vmul(m[q], xr[LA * LA + i][c]);
+                else vfma(tk[k][c], m[q], xr[LA * LA + i][c]);
+            }
+        });
+        static_for<NC>([&](auto kc) {
+            constexpr int k = decltype(kc)::value;
+            if constexpr (has_k<LI, LSH, LO>(T, k)) {
+#pragma unroll
+                for (int c = 0; c < NV; ++c) vfma(acc[LC * LC + k][c], wv[c], tk[k][c]);
+            }
+        });
+    }
+}
+
+template <int CPT, bool PK>
+__device__ __forceinline__ void store_lane(float *p, const typename LaneVec<CPT, PK>::V (&v)[LaneVec<CPT, PK>::NV]) {
+    if constexpr (!LaneVec<CPT, PK>::kPair) store_vec<CPT>(p, v);
+    else if constexpr (CPT == 4) *reinterpret_cast<ulonglong2 *>(p) = make_ulonglong2(v[0], v[1]);
+    else *reinterpret_cast<f32x2 *>(p) = v[0];
+}
+
+// CPT channels per lane (mul = 32*CPT), PK: packed pairs of channels. The
+// register cap follows from MINB (blocks of 256 threads per SM).
+template <int LI, int LSH, int LO, int CPT, bool PK, int MINB, typename FT>
+__global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(const __grid_constant__ RingParams prm) {
+    using LV = LaneVec<CPT, PK>;
+    using V = typename LV::V;
+    constexpr int NV = LV::NV;
+    constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
+    constexpr int RI = rows_upto(LI), RO = rows_upto(LO);
+    constexpr int KR = (P.R + 31) / 32;
+    constexpr int MUL = 32 * CPT;
+    constexpr int DX = RI * MUL, DOUT = RO * MUL, SHN = rows_upto(LSH);
+    constexpr int WNUM = P.n * MUL;
+    constexpr int WB = WNUM * (int)sizeof(FT), FB = DX * (int)sizeof(FT);
+    constexpr int MS = LV::kPair ? 2 * P.R : P.R;  // M floats per edge
+    static_assert(WB % 16 == 0 && FB % 16 == 0, "bulk copies move 16-byte multiples");
+    extern __shared__ __align__(128) unsigned char smem[];
+    static_assert(MS % 4 == 0, "M rows are read with 16-byte loads");
+    // block-shared recipe of the M entries: r -> {4*j0, 4*j1, c0, c1},
+    // M[r] = c0 * sh[j0] + c1 * sh[j1]
+    int4 *tab = reinterpret_cast<int4 *>(smem);
+    for (int r = threadIdx.x; r < P.R; r += blockDim.x)
+        tab[r] = make_int4((int)(prm.ej[r] & 0xffffu) * 4, (int)(prm.ej[r] >> 16) * 4, __float_as_int(prm.ec[r][0]),
+                           __float_as_int(prm.ec[r][1]));
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + wib;
+    if (gw >= prm.n_warps) return;
+    const int S = prm.S, eps = prm.eps;
+    unsigned char *base = smem + prm.tab_bytes + (size_t)wib * prm.warp_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + prm.bar_off);
+    int4 *meta = reinterpret_cast<int4 *>(base + prm.meta_off);
+    float *Mw = reinterpret_cast<float *>(base + prm.m_off);
+    if (lane == 0)
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], prm.x_lsu ? 33 : 1);  // + one arrival per lane
+    fence_barrier_init();
+    __syncwarp();
+
+    const int nP = prm.n_pieces, nW = prm.n_warps, N = prm.n_dst;
+    const int64_t E = prm.E;
+    const int32_t *rp = prm.row_ptr;
+    const int32_t *srcp = prm.src;
+    const FT *xp = static_cast<const FT *>(prm.x);
+    const FT *wp = static_cast<const FT *>(prm.w);
+    const int ch0 = lane * CPT;
+    auto piece_lo = [&](int p) -> int64_t { return (int64_t)p * E / nP; };
+
+    // ---- issue side: chunk cursors over this warp's pieces -------------------------
+    struct Cur {
+        int p;
+        int64_t e, hi;
+    };
+    auto normalize = [&](Cur &c) {
+        while (c.p < nP && c.e >= c.hi) {
+            c.p += nW;
+            if (c.p < nP) {
+                c.e = piece_lo(c.p);
+                c.hi = piece_lo(c.p + 1);
+            }
+        }
+    };
+    auto chunk_n = [&](const Cur &c) -> int {
+        return c.p < nP ? (int)min((int64_t)eps, c.hi - c.e) : 0;
+    };
+    auto load_src = [&](const Cur &c) -> int {
+        return lane < chunk_n(c) ? srcp[c.e + lane] : -1;
+    };
+    Cur ic{gw, gw < nP ? piece_lo(gw) : 0, gw < nP ? piece_lo(gw + 1) : 0};
+    normalize(ic);
+    Cur lc = ic;  // one chunk ahead of ic
+    lc.e += chunk_n(lc);
+    normalize(lc);
+    int srcA = load_src(ic), srcB = load_src(lc);
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    const int64_t sh_bytes_all = E * SHN * 4;
+    int n_issued = 0, s_iss = 0;
+    auto issue_next = [&]() {
+        const int n = chunk_n(ic);
+        if (n == 0) return;
+        const int s = s_iss;
+        s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
+        const bool ok = lane < n && (uint32_t)srcA < (uint32_t)prm.n_src;
+        const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0 && okmask != (n == 32 ? 0xffffffffu : (1u << n) - 1u)) set_status(prm.status, TP_DEV_ERR_INDEX);
+        unsigned char *sb = base + (size_t)s * prm.stage_bytes;
+        // harmonic rows [e, e+n): the 16-byte aligned span around them by one bulk
+        // copy; a piece past the array's last 16-byte boundary by plain loads
+        const int64_t b0 = ic.e * SHN * 4, b1 = (ic.e + n) * SHN * 4;
+        const int64_t a0 = b0 & ~(int64_t)15;
+        int64_t a1 = (b1 + 15) & ~(int64_t)15;
+        if (a1 > sh_bytes_all) a1 = sh_bytes_all & ~(int64_t)15;
+        if (a1 < a0) a1 = a0;
+        const uint32_t sh_tma = (uint32_t)(a1 - a0);
+        if (a1 < b1) {
+            const float *sf = prm.sh + a1 / 4;
+            float *df = reinterpret_cast<float *>(sb + prm.sh_off) + (a1 - a0) / 4;
+            for (int q = lane; q < (int)((b1 - a1) / 4); q += 32) df[q] = sf[q];
+        }
+        const uint32_t bytes = (uint32_t)n * WB + (prm.x_lsu ? 0u : (uint32_t)__popc(okmask) * FB) + sh_tma;
+        if (lane == 0) {
+            meta[s] = make_int4(n, (int)okmask, (int)((b0 - a0) / 4), 0);
+            mbar_arrive_expect_tx(&full[s], bytes);
+        }
+        __syncwarp();
+        if (lane == 0) bulk_g2s(sb, wp + ic.e * WNUM, (uint32_t)n * WB, &full[s], pol_stream);
+        if (lane == 1 && sh_tma > 0)
+            bulk_g2s(sb + prm.sh_off, reinterpret_cast<const unsigned char *>(prm.sh) + a0, sh_tma, &full[s],
+                     pol_stream);
+        if (prm.x_lsu) {
+            // row q: lane l moves bytes [16 l, 16 l + 16) (+512 ...) of x[src]
+            for (int q = 0; q < n; ++q) {
+                const int r = __shfl_sync(0xffffffffu, srcA, q);
+                if (!((okmask >> q) & 1u)) continue;
+                const unsigned char *xs = reinterpret_cast<const unsigned char *>(xp + (int64_t)r * DX);
+                unsigned char *xd = sb + prm.f_off + q * FB;
+#pragma unroll
+                for (int o = lane * 16; o < FB; o += 512) cp_async16(xd + o, xs + o);
+            }
+            cp_async_mbar_arrive_noinc(&full[s]);
+        } else if (ok) {
+            bulk_g2s(sb + prm.f_off + lane * FB, xp + (int64_t)srcA * DX, (uint32_t)FB, &full[s], pol_keep);
+        }
+        ++n_issued;
+        ic = lc;
+        srcA = srcB;
+        lc.e += chunk_n(lc);
+        normalize(lc);
+        srcB = load_src(lc);
+    };
+    for (int k = 0; k < S; ++k) issue_next();
+
+    // ---- destination ranges of this warp's pieces -------------------------------
+    // F(e) = smallest d with row_ptr[d] >= e. Piece p covers destinations
+    // [F(lo(p)) (-1 if that one starts before lo(p)), F(lo(p+1))), the last piece up to N.
+    const int np_w = gw < nP ? (nP - 1 - gw) / nW + 1 : 0;
+    int fb = 0;  // lane i < 2*np_w: F(lo(p_{i/2} + (i&1)))
+    if (np_w == 1) {
+        const int f0 = warp_first_geq(rp, N, piece_lo(gw), lane);
+        const int f1 = warp_first_geq(rp, N, piece_lo(gw + 1), lane);
+        fb = lane == 0 ? f0 : f1;
+    } else if (lane < 2 * np_w) {
+        fb = lane_first_geq(rp, N, piece_lo(gw + (lane >> 1) * nW + (lane & 1)));
+    }
+
+    // ---- consume side ---------------------------------------------------------------
+    V acc[RO][NV];
+#pragma unroll
+    for (int r = 0; r < RO; ++r)
+#pragma unroll
+        for (int c = 0; c < NV; ++c) acc[r][c] = V(0);
+    int n_done = 0, s_done = 0;
+    uint32_t ph_done = 0;
+    bool failed = false;
+    for (int j = 0; j < np_w && !failed; ++j) {
+        const int p = gw + j * nW;
+        const int64_t e_lo = piece_lo(p), e_hi = piece_lo(p + 1);
+        int d_start = __shfl_sync(0xffffffffu, fb, 2 * j);
+        int d_end = __shfl_sync(0xffffffffu, fb, 2 * j + 1);
+        if (d_start > N) d_start = N;
+        if (d_start > 0 && (int64_t)rp[d_start] > e_lo) d_start -= 1;
+        if (p == nP - 1 || d_end > N) d_end = N;
+        if (d_end < d_start) d_end = d_start;
+        const int head_dst = (d_start < d_end && (int64_t)rp[d_start] < e_lo) ? d_start : -1;
+        int tail_dst = (p < nP - 1 && d_end > d_start && (int64_t)rp[d_end] > e_hi) ? d_end - 1 : -1;
+        if (tail_dst == head_dst) tail_dst = -1;
+        if (lane == 0) {
+            prm.carry_dst[2 * p] = head_dst;
+            prm.carry_dst[2 * p + 1] = tail_dst;
+        }
+        // row_ptr window: lane l holds rp[wbase + l]
+        int wbase = d_start;
+        int32_t wv = (wbase + lane <= N) ? rp[wbase + lane] : 0;
+        auto rp_get = [&](int d) -> int64_t {
+            if (d < wbase || d >= wbase + 32) {
+                wbase = d;
+                wv = (wbase + lane <= N) ? rp[wbase + lane] : 0;
+            }
+            return (int64_t)__shfl_sync(0xffffffffu, wv, d - wbase);
+        };
+        int cur_d = d_start;
+        int64_t seg_end = 0;
+        auto enter = [&](int d) {
+            if (d >= d_end) return;
+            int64_t a = rp_get(d), b = rp_get(d + 1);
+            if (a < 0 || b < a || b > E) {
+                if (lane == 0) set_status(prm.status, TP_DEV_ERR_SEGMENT);
+                b = a < 0 ? 0 : (a > E ? E : a);
+            }
+            seg_end = b < e_hi ? b : e_hi;
+        };
+        auto store_row = [&](int d) {
+            float *orow;
+            if (d == head_dst) orow = prm.carry + (int64_t)(2 * p) * DOUT;
+            else if (d == tail_dst) orow = prm.carry + (int64_t)(2 * p + 1) * DOUT;
+            else orow = prm.out + (int64_t)d * DOUT;
+            orow += ch0;
+#pragma unroll
+            for (int r = 0; r < RO; ++r) store_lane<CPT, PK>(orow + r * MUL, acc[r]);
+#pragma unroll
+            for (int r = 0; r < RO; ++r)
+#pragma unroll
+                for (int c = 0; c < NV; ++c) acc[r][c] = V(0);
+        };
+        enter(cur_d);
+        int64_t e = e_lo;
+        while (e < e_hi) {
+            const int s = s_done;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph_done))) {
+                if (lane == 0) set_status(prm.status, TP_DEV_ERR_TIMEOUT);
+                failed = true;
+                break;
+            }
+            const int4 mt = meta[s];
+            const int n = mt.x;
+            const uint32_t vmask = (uint32_t)mt.y;
+            const unsigned char *sb = base + (size_t)s * prm.stage_bytes;
+            const float *shs = reinterpret_cast<const float *>(sb + prm.sh_off) + mt.z;
+#pragma unroll
+            for (int k = 0; k < KR; ++k) {
+                const int r = lane + 32 * k;
+                if (r < P.R) {
+                    const int4 t = tab[r];
+                    const unsigned char *shb = reinterpret_cast<const unsigned char *>(shs);
+                    float *mo = Mw + (LV::kPair ? 2 * r : r);
+                    for (int q = 0; q < n; ++q) {
+                        const float v = fmaf(__int_as_float(t.z), *reinterpret_cast<const float *>(shb + t.x),
+                                             __int_as_float(t.w) * *reinterpret_cast<const float *>(shb + t.y));
+                        if constexpr (LV::kPair) *reinterpret_cast<float2 *>(mo) = make_float2(v, v);
+                        else *mo = v;
+                        shb += SHN * 4;
+                        mo += MS;
+                    }
+                }
+            }
+            __syncwarp();
+            const FT *wl = reinterpret_cast<const FT *>(sb) + ch0;
+            const FT *xl = reinterpret_cast<const FT *>(sb + prm.f_off) + ch0;
+            for (int q = 0; q < n; ++q, ++e) {
+                while (e >= seg_end && cur_d < d_end) {
+                    store_row(cur_d);
+                    ++cur_d;
+                    enter(cur_d);
+                }
+                if (!((vmask >> q) & 1u)) continue;
+                const FT *xq = xl + q * (FB / (int)sizeof(FT));
+                V xr[RI][NV];
+#pragma unroll
+                for (int r = 0; r < RI; ++r) load_lane<CPT, PK>(xq + r * MUL, xr[r]);
+                const FT *wq = wl + q * (WB / (int)sizeof(FT));
+                const float *Mq = Mw + q * MS;
+                static_for<P.n>([&](auto tc) {
+                    ring_path<LI, LSH, LO, decltype(tc)::value, CPT, PK, FT>(acc, xr, wq, Mq);
+                });
+            }
+            // this warp's reads of the stage come before the bulk copies that refill it
+            fence_proxy_async_smem();
+            __syncwarp();
+            issue_next();
+            ++n_done;
+            if (++s_done == S) {
+                s_done = 0;
+                ph_done ^= 1u;
+            }
+        }
+        if (failed) break;
+        while (cur_d < d_end) {
+            store_row(cur_d);
+            ++cur_d;
+            enter(cur_d);
+        }
+    }
+    if (failed) {
+        // let the copies still in flight land before the shared memory is released
+        for (int k = n_done; k < n_issued; ++k) {
+            (void)mbar_wait(&full[s_done], ph_done);
+            if (++s_done == S) {
+                s_done = 0;
+                ph_done ^= 1u;
+            }
+        }
+    }
+}
+
+}  // namespace tpc

@@ -158,9 +158,10 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
     const int CS = prm.consumers;
     if (threadIdx.x == 0)
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 33);
-            mbar_init(&ready[s], 32);
-            mbar_init(&empty[s], 32 * CS);
+            // one arrival per warp: per-thread arrivals on one barrier word serialise
+            mbar_init(&full[s], 1);
+            mbar_init(&ready[s], 1);
+            mbar_init(&empty[s], CS);
         }
     fence_barrier_init();
     __syncthreads();
@@ -291,8 +292,21 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
             unsigned char *sb = stages + s * L.stage_bytes;
             float *shs = reinterpret_cast<float *>(sb + L.sh_off);
             const int shn = L.sh_floats;
-            const float *shsrc = prm.sh + (int64_t)m.e0 * shn;
-            for (int q = lane; q < m.n * shn; q += 32) cp_async4(shs + q, shsrc + q);
+            // harmonic rows [e0, e0+n): one bulk copy of the 16-byte aligned span
+            // around them; a tail that would run past the array end is copied with
+            // plain loads instead. shs[sh_lead + q*shn + j] is component j of edge e0+q.
+            const int64_t b0 = (int64_t)m.e0 * shn * 4, b1 = ((int64_t)m.e0 + m.n) * shn * 4;
+            const int64_t sh_bytes = E * shn * 4;
+            const int64_t a0 = b0 & ~(int64_t)15;
+            int64_t a1 = (b1 + 15) & ~(int64_t)15;
+            if (a1 > sh_bytes) a1 = sh_bytes & ~(int64_t)15;
+            if (a1 < a0) a1 = a0;
+            const uint32_t sh_tma = m.n > 0 ? (uint32_t)(a1 - a0) : 0u;
+            if (m.n > 0 && a1 < b1) {
+                const float *srcf = prm.sh + a1 / 4;
+                float *dstf = shs + (a1 - a0) / 4;
+                for (int q = lane; q < (int)((b1 - a1) / 4); q += 32) dstf[q] = srcf[q];
+            }
             if (prm.copy_mode == 1) {
                 // every lane moves 16-byte pieces of the weight rows and of each gathered x row;
                 // the range checks only guard against a broken launch (they never fire on valid input)
@@ -315,18 +329,21 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
                         cp_async16(sb + L.f_off + q * L.f_bytes + o, xsrc + o);
                 }
             }
-            cp_async_mbar_arrive_noinc(&full[s]);
-            const uint32_t bytes = prm.copy_mode == 1 ? 0u :
-                (uint32_t)__popc(okmask) * (uint32_t)L.f_bytes + (uint32_t)m.n * (uint32_t)L.w_bytes;
+            if (prm.copy_mode == 1) cp_async_mbar_arrive_noinc(&full[s]);
+            const uint32_t bytes = sh_tma + (prm.copy_mode == 1 ? 0u :
+                (uint32_t)__popc(okmask) * (uint32_t)L.f_bytes + (uint32_t)m.n * (uint32_t)L.w_bytes);
+            __syncwarp();
             if (lane == 0) {
                 ChunkMeta mm = m;
                 mm.bits |= okmask << 8;
+                mm.seg_lead = (int32_t)((b0 - a0) / 4);
                 meta[s] = mm;
                 mbar_arrive_expect_tx(&full[s], bytes);
             }
+            __syncwarp();
+            if (lane == 0 && sh_tma > 0)
+                bulk_g2s(shs, reinterpret_cast<const unsigned char *>(prm.sh) + a0, sh_tma, &full[s], pol_stream);
             if (prm.copy_mode == 0) {
-                fence_proxy_async_smem();
-                __syncwarp();
                 if (lane == 0 && m.n > 0)
                     bulk_g2s(sb + L.w_off, wp + (int64_t)m.e0 * prm.wnum, (uint32_t)(m.n * L.w_bytes), &full[s],
                              pol_stream);
@@ -341,7 +358,7 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
         for (int s = 0; s < S && !term_issued; ++s) issue(s);
         int n_built = 0;
         bool failed = false;
-        uint64_t t_idle = 0;
+        uint32_t idle = 0;
         for (;;) {
             bool did = false;
             if (n_built < n_issued) {
@@ -349,7 +366,8 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
                 if (__all_sync(0xffffffffu, mbar_test_wait(&full[s], (n_built / S) & 1))) {
                     const ChunkMeta m = meta[s];
                     if (m.bits & kValid) {
-                        const float *shs = reinterpret_cast<const float *>(stages + s * L.stage_bytes + L.sh_off);
+                        const float *shs = reinterpret_cast<const float *>(stages + s * L.stage_bytes + L.sh_off) +
+                                           m.seg_lead;
                         float *Mq = Mst + s * L.eps * P.R;
                         for (int q = 0; q < m.n; ++q) {
                             const float *shq = shs + q * L.sh_floats;
@@ -362,7 +380,7 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
                         }
                     }
                     __syncwarp();
-                    mbar_arrive(&ready[s]);
+                    if (lane == 0) mbar_arrive(&ready[s]);
                     ++n_built;
                     if (!(m.bits & kValid)) break;  // terminator handed to the consumers
                     did = true;
@@ -376,12 +394,10 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
                 }
             }
             if (did) {
-                t_idle = 0;
+                idle = 0;
             } else {
-                const uint64_t now = global_ns();
-                if (t_idle == 0) t_idle = now;
-                else if (now - t_idle > kWaitLimitNs) { failed = true; break; }
-                __nanosleep(32);
+                if (++idle > kWaitProbes) { failed = true; break; }
+                if (idle > 32) __nanosleep(20);
             }
         }
         if (failed) {
@@ -443,7 +459,7 @@ __global__ void __launch_bounds__(32 * (kTeamMaxConsumers + 1)) team_fwd_kernel(
                 }
             }
             __syncwarp();
-            mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
     }
 }

@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include "direct_fwd.cuh"
+#include "ring_fwd.cuh"
 #include "team_fwd.cuh"
 
 namespace tpc {
@@ -15,6 +16,8 @@ const void *team_kernel_f32(int shape, int cpt);
 const void *team_kernel_bf16(int shape, int cpt);
 const void *direct_kernel_f32(int shape, int cpt);
 const void *direct_kernel_bf16(int shape, int cpt);
+const void *ring_kernel_f32(int shape, int cpt, int pk);
+const void *ring_kernel_bf16(int shape, int cpt, int pk);
 
 __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_t *__restrict__ carry_dst,
                                    int n_streams, int dim_out, float *__restrict__ out) {
@@ -58,10 +61,11 @@ static bool team_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int 
     const TeamPlan &TP = d->team;
     if (!TP.valid) return false;
     const int mul = d->tab.mul;
-    int cpt = env_int("TPCONV_TEAM_CPT", mul >= 128 ? 1 : 1);
-    if (cpt != 1 && cpt != 2) cpt = 1;
-    if (mul % (32 * cpt) != 0) cpt = 1;
     if (mul % 32 != 0) return false;
+    // default: one consumer warp covering every channel (fewest M reads per edge)
+    int cpt = env_int("TPCONV_TEAM_CPT", mul / 32 > 4 ? 4 : mul / 32);
+    if (cpt != 1 && cpt != 2 && cpt != 4) cpt = 1;
+    if (mul % (32 * cpt) != 0) return false;
     const int cs = mul / (32 * cpt);
     if (cs < 1 || cs > kTeamMaxConsumers) return false;
     tl.fn = dtype == TP_F32 ? team_kernel_f32(TP.shape, cpt) : team_kernel_bf16(TP.shape, cpt);
@@ -72,17 +76,19 @@ static bool team_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int 
     L.f_bytes = d->tab.dim_x * esz;
     L.sh_floats = d->tab.dim_sh;
     const int per_edge = L.w_bytes + L.f_bytes + L.sh_floats * 4;
-    int eps = env_int("TPCONV_TEAM_STAGE_BYTES", 6144) / per_edge;
+    // chunks of >= ~16 KB: the producer's per-chunk work is amortised over several edges
+    const int target = env_int("TPCONV_TEAM_STAGE_BYTES", 16384);
+    int eps = (target + per_edge - 1) / per_edge;
     eps = eps < 1 ? 1 : (eps > 8 ? 8 : eps);
-    L.S = env_int("TPCONV_TEAM_STAGES", 3);
-    if (L.S < 2 || L.S > kTeamMaxStages) L.S = 4;
+    L.S = env_int("TPCONV_TEAM_STAGES", 2);
+    if (L.S < 2 || L.S > kTeamMaxStages) L.S = 2;
     L.eps = eps;
     L.R = TP.R;
     L.nnz = TP.nnz;
     L.w_off = 0;
     L.f_off = eps * L.w_bytes;
     L.sh_off = L.f_off + eps * L.f_bytes;
-    L.stage_bytes = round_up(L.sh_off + eps * L.sh_floats * 4, 128);
+    L.stage_bytes = round_up(L.sh_off + eps * L.sh_floats * 4 + 32, 128);  // +32: aligned harmonic span
     L.tab_off = 0;
     L.bar_off = 0;
     L.meta_off = L.bar_off + 3 * L.S * 8;
@@ -150,6 +156,85 @@ static bool direct_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, Di
     return true;
 }
 
+struct RingLaunch {
+    const void *fn = nullptr;
+    RingParams geo{};  // layout fields only
+    int wpb = 0, n_warps = 0, n_pieces = 0, smem = 0;
+};
+
+// One warp covers all channels, CPT = mul/32 in {1,2,4} channels per lane,
+// for descriptors in the natural layout the kernel is compiled for.
+// Tunables (environment): TPCONV_RING_STAGE_BYTES (target bytes per chunk),
+// TPCONV_RING_STAGES, TPCONV_RING_WARPS (warps per block), TPCONV_RING_ROUNDS
+// (pieces per warp), TPCONV_RING_PACK (packed channel pairs, CPT >= 2),
+// TPCONV_RING_XLSU (gathered rows by cp.async instead of bulk copies).
+static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin, RingLaunch &rl) {
+    const TeamPlan &TP = d->team;
+    if (!TP.valid) return false;
+    const Tables &T = d->tab;
+    const int mul = T.mul;
+    if (mul % 32 != 0) return false;
+    const int cpt = mul / 32;
+    if (cpt != 1 && cpt != 2 && cpt != 4) return false;
+    const int pk = cpt >= 2 ? env_int("TPCONV_RING_PACK", cpt == 2 ? 1 : 0) != 0 : 0;
+    // natural layout: block l at l*l*mul, paths in program order
+    const ProgShape shp = kProgShapes[TP.shape];
+    const Program prog = make_natural_program(shp.li, shp.lsh, shp.lo);
+    if (T.dim_x != (shp.li + 1) * (shp.li + 1) * mul || T.dim_out != (shp.lo + 1) * (shp.lo + 1) * mul ||
+        T.dim_sh != (shp.lsh + 1) * (shp.lsh + 1) || T.wnum != prog.n * mul || TP.R != prog.R)
+        return false;
+    for (int l = 0; l <= shp.li; ++l)
+        if (T.x_off[l] != l * l * mul) return false;
+    for (int l = 0; l <= shp.lo; ++l)
+        if (T.o_off[l] != l * l * mul) return false;
+    for (int t = 0; t < prog.n; ++t)
+        if (TP.wofs[t] != t * mul) return false;
+    rl.fn = dtype == TP_F32 ? ring_kernel_f32(TP.shape, cpt, pk) : ring_kernel_bf16(TP.shape, cpt, pk);
+    if (!rl.fn) return false;
+    const int esz = dtype == TP_F32 ? 4 : 2;
+    RingParams &g = rl.geo;
+    const int w_bytes = T.wnum * esz, f_bytes = T.dim_x * esz;
+    const int shn = T.dim_sh;
+    const int per_edge = w_bytes + f_bytes + shn * 4;
+    // about 4.5 KB per chunk and two stages per warp: one chunk lands while the
+    // warp works on the other, and enough warps fit on an SM to keep HBM busy
+    const int target = env_int("TPCONV_RING_STAGE_BYTES", 4500);
+    int eps = (target + per_edge - 1) / per_edge;
+    eps = eps < 1 ? 1 : (eps > 32 ? 32 : eps);
+    int S = env_int("TPCONV_RING_STAGES", 2);
+    S = S < 2 ? 2 : (S > 8 ? 8 : S);
+    g.S = S;
+    g.eps = eps;
+    g.f_off = eps * w_bytes;
+    g.sh_off = g.f_off + eps * f_bytes;
+    g.stage_bytes = round_up(g.sh_off + eps * shn * 4 + 32, 128);  // +32: 16-byte aligned harmonic span
+    g.m_off = S * g.stage_bytes;
+    g.meta_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
+    g.bar_off = round_up(g.meta_off + S * 16, 8);
+    g.warp_bytes = round_up(g.bar_off + S * 8, 128);
+    g.tab_bytes = round_up(16 * TP.R, 128);
+    g.x_lsu = env_int("TPCONV_RING_XLSU", 0) != 0;
+    int wpb = env_int("TPCONV_RING_WARPS", 8);
+    wpb = wpb < 1 ? 1 : (wpb > kRingMaxWarps ? kRingMaxWarps : wpb);
+    while (wpb > 1 && g.tab_bytes + wpb * g.warp_bytes > smem_optin) --wpb;
+    rl.smem = g.tab_bytes + wpb * g.warp_bytes;
+    if (rl.smem > smem_optin) return false;
+    rl.wpb = wpb;
+    if (cudaFuncSetAttribute(rl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess) return false;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rl.fn, 32 * wpb, rl.smem) != cudaSuccess || occ < 1)
+        return false;
+    long long nw = (long long)sms * occ * wpb;
+    const long long by_edges = (E + 63) / 64;  // at least ~64 edges per warp
+    if (nw > by_edges) nw = by_edges;
+    if (nw < 1) nw = 1;
+    int rounds = env_int("TPCONV_RING_ROUNDS", 1);
+    rounds = rounds < 1 ? 1 : (rounds > kRingMaxPiecesPerWarp ? kRingMaxPiecesPerWarp : rounds);
+    rl.n_warps = (int)nw;
+    rl.n_pieces = (int)nw * rounds;
+    return true;
+}
+
 // Kernel choice: rows of 32 channels (one warp per stream, small per-edge
 // rows) stream best through the per-warp ring; wider rows through the CTA
 // pipeline whose consumers split the channels. TPCONV_FWD_PIPELINED=0/1 forces
@@ -161,7 +246,18 @@ static bool use_direct(const tp_desc *d) {
     return d->tab.mul <= 32;
 }
 
+// The warp-ring kernel is the default; TPCONV_FWD_KERNEL=team|direct selects
+// the older kernels.
+static bool use_ring() {
+    const char *v = std::getenv("TPCONV_FWD_KERNEL");
+    return !(v && (std::strcmp(v, "team") == 0 || std::strcmp(v, "direct") == 0));
+}
+
 size_t team_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin) {
+    if (use_ring()) {
+        RingLaunch rl;
+        if (ring_plan(d, dtype, E, sms, smem_optin, rl)) return carry_bytes(rl.n_pieces, d->tab.dim_out);
+    }
     if (use_direct(d)) {
         DirectLaunch dl;
         if (!direct_plan(d, dtype, E, sms, dl)) return 0;
@@ -224,6 +320,48 @@ static cudaError_t direct_forward(const tp_desc *d, tp_dtype dtype, const void *
     return cudaGetLastError();
 }
 
+static cudaError_t ring_forward(const tp_desc *d, const RingLaunch &rl0, const void *x, const float *sh,
+                                const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src,
+                                int32_t N_dst, int64_t E, float *out, void *ws, size_t ws_bytes, int *status,
+                                cudaStream_t stream) {
+    RingLaunch rl = rl0;
+    const Tables &T = d->tab;
+    const int rounds = rl.n_pieces / rl.n_warps;
+    // a smaller caller workspace: fewer warps
+    while (rl.n_warps > 1 && carry_bytes(rl.n_warps * rounds, T.dim_out) > ws_bytes) rl.n_warps = (rl.n_warps + 1) / 2;
+    rl.n_pieces = rl.n_warps * rounds;
+    if (!ws || carry_bytes(rl.n_pieces, T.dim_out) > ws_bytes) return cudaErrorNotSupported;
+    static_assert(sizeof(RingParams) < 32000, "kernel parameter block too large");
+    RingParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm = rl.geo;
+    std::memcpy(prm.ej, d->team.ej, sizeof(uint32_t) * d->team.R);
+    std::memcpy(prm.ec, d->team.ec, sizeof(float) * 2 * d->team.R);
+    prm.x = x;
+    prm.sh = sh;
+    prm.w = w;
+    prm.src = src;
+    prm.row_ptr = row_ptr;
+    prm.out = out;
+    prm.carry = static_cast<float *>(ws);
+    const size_t cb = ((size_t)2 * rl.n_pieces * T.dim_out * sizeof(float) + 255) / 256 * 256;
+    prm.carry_dst = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(ws) + cb);
+    prm.status = status;
+    prm.n_src = N_src;
+    prm.n_dst = N_dst;
+    prm.n_warps = rl.n_warps;
+    prm.n_pieces = rl.n_pieces;
+    prm.E = E;
+    const int blocks = (rl.n_warps + rl.wpb - 1) / rl.wpb;
+    void *args[] = {&prm};
+    cudaError_t e = cudaLaunchKernel(rl.fn, dim3(blocks), dim3(32 * rl.wpb), args, (size_t)rl.smem, stream);
+    if (e != cudaSuccess) return e;
+    const int wpb = 8;
+    carry_fixup_kernel<<<(rl.n_pieces + wpb - 1) / wpb, 32 * wpb, 0, stream>>>(prm.carry, prm.carry_dst, rl.n_pieces,
+                                                                                T.dim_out, out);
+    return cudaGetLastError();
+}
+
 // Launches the program kernel (+ partial merge). Returns cudaErrorNotSupported
 // when the descriptor has no program kernel or the workspace cannot hold one
 // stream's partials (the caller then uses the generic kernel).
@@ -232,11 +370,19 @@ cudaError_t team_forward(const tp_desc *d, tp_dtype dtype, const void *x, const 
                          float *out, void *ws, size_t ws_bytes, int sms, int smem_optin, int *status,
                          cudaStream_t stream) {
     if (env_int("TPCONV_DISABLE_TEAM", 0)) return cudaErrorNotSupported;
+    if (use_ring()) {
+        RingLaunch rl;
+        const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
+                             reinterpret_cast<uintptr_t>(sh);
+        if ((al & 15u) == 0 && ring_plan(d, dtype, E, sms, smem_optin, rl))
+            return ring_forward(d, rl, x, sh, w, src, row_ptr, N_src, N_dst, E, out, ws, ws_bytes, status, stream);
+    }
     if (use_direct(d))
         return direct_forward(d, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, ws, ws_bytes, sms, status,
                               stream);
     TeamLaunch tl;
     if (!team_plan(d, dtype, E, sms, smem_optin, tl)) return cudaErrorNotSupported;
+    if (reinterpret_cast<uintptr_t>(sh) & 15u) return cudaErrorNotSupported;  // bulk copies of harmonic rows
     int streams = tl.streams;
     while (streams > 0 && carry_bytes(streams, d->tab.dim_out) > ws_bytes) streams >>= 1;
     if (streams < 1 || !ws) return cudaErrorNotSupported;

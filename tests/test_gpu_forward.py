@@ -116,19 +116,62 @@ def test_bipartite_sources(tpc):
     assert err(out, oracle_forward(prob)) <= FP32_TOL
 
 
-@pytest.mark.parametrize("pipelined", ["0", "1"], ids=["ring", "cta-pipeline"])
+KERNELS = {
+    "warp-ring": {},                                                        # default
+    "warp-cpasync": {"TPCONV_FWD_KERNEL": "direct", "TPCONV_FWD_PIPELINED": "0"},
+    "cta-pipeline": {"TPCONV_FWD_KERNEL": "team", "TPCONV_FWD_PIPELINED": "1"},
+}
+
+
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("irr,dtype", [(SHAPES[0], torch.float32), (SHAPES[1], torch.float32),
                                        (SHAPES[2], torch.bfloat16), (SHAPES[3], torch.float32)],
                          ids=["tiny", "medium", "large-bf16", "lesson"])
-def test_both_split_kernels(tpc, monkeypatch, irr, dtype, pipelined):
-    """Both edge-balanced kernels (the per-warp cp.async ring and the CTA
-    pipeline with a TMA producer warp) against the oracle, whichever the
-    library would pick by default."""
-    monkeypatch.setenv("TPCONV_FWD_PIPELINED", pipelined)
+def test_all_split_kernels(tpc, monkeypatch, irr, dtype, kernel):
+    """Every edge-balanced kernel (the warp-private TMA ring, the warp-private
+    cp.async ring and the CTA pipeline with a producer warp) against the oracle."""
+    for k, v in KERNELS[kernel].items():
+        monkeypatch.setenv(k, v)
     prob = make_problem(*irr, n_src=400, n_dst=333, E=9000, seed=14)
     out, _, _ = run(tpc, prob, dtype)
-    tol = FP32_TOL
-    assert err(out, oracle_forward(prob, dtype)) <= tol
+    assert err(out, oracle_forward(prob, dtype)) <= FP32_TOL
+    assert tpc.tp_device_status(reset=True) == 0
+
+
+RING_GEOMETRIES = {
+    "eps1-S2-w1": {"TPCONV_RING_STAGE_BYTES": "1", "TPCONV_RING_STAGES": "2", "TPCONV_RING_WARPS": "1"},
+    "eps32-S2": {"TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_STAGES": "2"},
+    "S8-w8": {"TPCONV_RING_STAGES": "8", "TPCONV_RING_WARPS": "8", "TPCONV_RING_STAGE_BYTES": "4096"},
+    "rounds3": {"TPCONV_RING_ROUNDS": "3"},
+    "rounds16-eps5": {"TPCONV_RING_ROUNDS": "16", "TPCONV_RING_STAGE_BYTES": "5000"},
+    "xlsu-eps32": {"TPCONV_RING_XLSU": "1", "TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_STAGES": "2"},
+    "xlsu-pack": {"TPCONV_RING_XLSU": "1", "TPCONV_RING_PACK": "1"},
+    "nopack": {"TPCONV_RING_PACK": "0"},
+}
+
+
+@pytest.mark.parametrize("geo", list(RING_GEOMETRIES))
+@pytest.mark.parametrize("irr,dtype", [(SHAPES[0], torch.float32), (SHAPES[1], torch.float32),
+                                       (SHAPES[2], torch.bfloat16)], ids=["cpt1", "cpt4", "cpt2-bf16"])
+def test_ring_geometries(tpc, monkeypatch, irr, dtype, geo):
+    """The warp ring with chunks of 1 to 32 edges, 2 to 8 stages, 1 to 8 warps
+    per block, several pieces per warp, gathered rows by bulk copies or by
+    cp.async, packed or scalar FMAs, on a graph with a 1000-edge
+    destination (cut across many pieces), empty destinations and a ragged tail."""
+    for k, v in RING_GEOMETRIES[geo].items():
+        monkeypatch.setenv(k, v)
+    rng = np.random.default_rng(21)
+    n_dst = 500
+    dst = np.concatenate([np.full(1000, 7), rng.integers(0, n_dst // 2, 5003) * 2, [n_dst - 1]])
+    rng.shuffle(dst)
+    prob = make_problem(*irr, n_src=300, n_dst=n_dst, E=len(dst), seed=22, dst=dst)
+    out, _, _ = run(tpc, prob, dtype)
+    ref = oracle_forward(prob, dtype)
+    on = out.double().cpu().numpy()
+    for d, c in zip(*np.unique(dst, return_counts=True)):
+        assert err(on[d], ref[d]) <= deg_tol(c), d
+    empty = np.setdiff1d(np.arange(n_dst), dst)
+    assert len(empty) > 100 and not out[torch.as_tensor(empty)].any()
     assert tpc.tp_device_status(reset=True) == 0
 
 
