@@ -10,11 +10,10 @@
 
 namespace tpc {
 
-// An mbarrier wait gives up after this many probes (each followed, after the
-// first few, by a ~20 ns sleep: about a second in all), so a lost copy turns
-// into a status bit instead of a hung GPU. Probes are counted rather than
-// timed: reading a clock in the wait loop sits on the critical path of every
-// handoff.
+// An mbarrier wait gives up after about this long, so a lost copy turns into a
+// status bit instead of a hung GPU.
+constexpr uint64_t kWaitNs = 1000000000ull;
+// Non-blocking probes of the producer loop that uses mbar_test_wait.
 constexpr uint32_t kWaitProbes = 1u << 25;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -79,13 +78,30 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Bounded wait: true when the phase completed, false after kWaitProbes probes.
+// Probe that may suspend the thread in hardware for up to about `hint_ns`
+// while the phase is incomplete (no issue slots spent spinning).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase completed, false after about kWaitNs.
+// The clock is read only once the phase was found incomplete, and then only
+// every 64 suspended probes.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitProbes; ++it) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if (it >= 32) __nanosleep(20);
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_hint(bar, parity, 2000u)) return true;
+        if ((it & 63u) == 0 && global_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 // Order this thread's earlier generic-proxy shared-memory accesses before

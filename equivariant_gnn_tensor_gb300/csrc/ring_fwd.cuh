@@ -16,8 +16,10 @@
 //   issue:   chunks of up to `eps` consecutive edges of its pieces, in order;
 //            one bulk copy for the chunk's weight rows, one for the 16-byte
 //            aligned span around its harmonic rows, one per edge for the
-//            gathered source row x[src[e]]. The source indices of the next two
-//            chunks are loaded ahead into registers.
+//            gathered source row x[src[e]] (each copy from its own lane, so
+//            all of them issue as one instruction). The source indices of the
+//            next two chunks are loaded ahead into registers; an out-of-range
+//            source sets a status bit and its edge gets a zero row.
 //   consume: wait for the chunk's stage, build the per-edge matrices
 //            M_p[i][k] = sum_j C_p[i,j,k] sh[j] (program layout, at most two
 //            terms per entry) into a warp-private buffer, then run every path as
@@ -39,11 +41,10 @@ constexpr int kRingMaxWarps = 8;
 constexpr int kRingMaxPiecesPerWarp = 16;
 
 struct RingParams {
-    int32_t S, eps;                      // stages per warp, edges per chunk (<= 32)
+    int32_t S, eps;                      // stages per warp, edges per chunk (<= 30)
     int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0, source rows, harmonic span
-    int32_t m_off, meta_off, bar_off, warp_bytes;  // warp region: stages, M, chunk meta, barriers
+    int32_t m_off, bar_off, warp_bytes;  // warp region: stages, M, barriers
     int32_t tab_bytes;                   // block-shared M recipe table at the start of shared memory
-    int32_t x_lsu;                       // 1: gathered rows by 16-byte cp.async from all lanes, 0: one bulk copy each
     uint32_t ej[kMaxM];
     float ec[kMaxM][2];
     const void *x;
@@ -283,28 +284,30 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     const int S = prm.S, eps = prm.eps;
     unsigned char *base = smem + prm.tab_bytes + (size_t)wib * prm.warp_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(base + prm.bar_off);
-    int4 *meta = reinterpret_cast<int4 *>(base + prm.meta_off);
     float *Mw = reinterpret_cast<float *>(base + prm.m_off);
     if (lane == 0)
-        for (int s = 0; s < S; ++s) mbar_init(&full[s], prm.x_lsu ? 33 : 1);  // + one arrival per lane
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
     __syncwarp();
 
     const int nP = prm.n_pieces, nW = prm.n_warps, N = prm.n_dst;
-    const int64_t E = prm.E;
+    const int E = (int)prm.E;  // the host launches this kernel only for E < 2^31
     const int32_t *rp = prm.row_ptr;
     const int32_t *srcp = prm.src;
     const FT *xp = static_cast<const FT *>(prm.x);
-    const FT *wp = static_cast<const FT *>(prm.w);
+    const unsigned char *wb = static_cast<const unsigned char *>(prm.w);
+    const unsigned char *shb_g = reinterpret_cast<const unsigned char *>(prm.sh);
     const int ch0 = lane * CPT;
-    auto piece_lo = [&](int p) -> int64_t { return (int64_t)p * E / nP; };
+    auto piece_lo = [&](int p) -> int { return (int)((int64_t)p * E / nP); };
 
     // ---- issue side: chunk cursors over this warp's pieces -------------------------
+    // A chunk is the next min(eps, hi - e) edges of the current piece; the
+    // consumer walks the same sequence, so nothing about a chunk but its data
+    // goes through shared memory.
     struct Cur {
-        int p;
-        int64_t e, hi;
+        int p, e, hi, n;
     };
-    auto normalize = [&](Cur &c) {
+    auto settle = [&](Cur &c) {  // skip finished pieces, then size the chunk
         while (c.p < nP && c.e >= c.hi) {
             c.p += nW;
             if (c.p < nP) {
@@ -312,74 +315,77 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                 c.hi = piece_lo(c.p + 1);
             }
         }
+        c.n = c.p < nP ? min(eps, c.hi - c.e) : 0;
     };
-    auto chunk_n = [&](const Cur &c) -> int {
-        return c.p < nP ? (int)min((int64_t)eps, c.hi - c.e) : 0;
-    };
-    auto load_src = [&](const Cur &c) -> int {
-        return lane < chunk_n(c) ? srcp[c.e + lane] : -1;
-    };
-    Cur ic{gw, gw < nP ? piece_lo(gw) : 0, gw < nP ? piece_lo(gw + 1) : 0};
-    normalize(ic);
+    auto load_src = [&](const Cur &c) -> int { return lane < c.n ? srcp[c.e + lane] : -1; };
+    Cur ic{gw, gw < nP ? piece_lo(gw) : 0, gw < nP ? piece_lo(gw + 1) : 0, 0};
+    settle(ic);
     Cur lc = ic;  // one chunk ahead of ic
-    lc.e += chunk_n(lc);
-    normalize(lc);
+    lc.e += lc.n;
+    settle(lc);
     int srcA = load_src(ic), srcB = load_src(lc);
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
-    const int64_t sh_bytes_all = E * SHN * 4;
+    const int64_t sh_bytes_all = (int64_t)E * SHN * 4;
     int n_issued = 0, s_iss = 0;
     auto issue_next = [&]() {
-        const int n = chunk_n(ic);
+        const int n = ic.n;
         if (n == 0) return;
         const int s = s_iss;
         s_iss = s_iss + 1 == S ? 0 : s_iss + 1;
-        const bool ok = lane < n && (uint32_t)srcA < (uint32_t)prm.n_src;
-        const uint32_t okmask = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0 && okmask != (n == 32 ? 0xffffffffu : (1u << n) - 1u)) set_status(prm.status, TP_DEV_ERR_INDEX);
-        unsigned char *sb = base + (size_t)s * prm.stage_bytes;
-        // harmonic rows [e, e+n): the 16-byte aligned span around them by one bulk
-        // copy; a piece past the array's last 16-byte boundary by plain loads
-        const int64_t b0 = ic.e * SHN * 4, b1 = (ic.e + n) * SHN * 4;
-        const int64_t a0 = b0 & ~(int64_t)15;
-        int64_t a1 = (b1 + 15) & ~(int64_t)15;
-        if (a1 > sh_bytes_all) a1 = sh_bytes_all & ~(int64_t)15;
-        if (a1 < a0) a1 = a0;
-        const uint32_t sh_tma = (uint32_t)(a1 - a0);
-        if (a1 < b1) {
-            const float *sf = prm.sh + a1 / 4;
-            float *df = reinterpret_cast<float *>(sb + prm.sh_off) + (a1 - a0) / 4;
-            for (int q = lane; q < (int)((b1 - a1) / 4); q += 32) df[q] = sf[q];
-        }
-        const uint32_t bytes = (uint32_t)n * WB + (prm.x_lsu ? 0u : (uint32_t)__popc(okmask) * FB) + sh_tma;
-        if (lane == 0) {
-            meta[s] = make_int4(n, (int)okmask, (int)((b0 - a0) / 4), 0);
-            mbar_arrive_expect_tx(&full[s], bytes);
-        }
-        __syncwarp();
-        if (lane == 0) bulk_g2s(sb, wp + ic.e * WNUM, (uint32_t)n * WB, &full[s], pol_stream);
-        if (lane == 1 && sh_tma > 0)
-            bulk_g2s(sb + prm.sh_off, reinterpret_cast<const unsigned char *>(prm.sh) + a0, sh_tma, &full[s],
-                     pol_stream);
-        if (prm.x_lsu) {
-            // row q: lane l moves bytes [16 l, 16 l + 16) (+512 ...) of x[src]
-            for (int q = 0; q < n; ++q) {
-                const int r = __shfl_sync(0xffffffffu, srcA, q);
-                if (!((okmask >> q) & 1u)) continue;
-                const unsigned char *xs = reinterpret_cast<const unsigned char *>(xp + (int64_t)r * DX);
-                unsigned char *xd = sb + prm.f_off + q * FB;
-#pragma unroll
-                for (int o = lane * 16; o < FB; o += 512) cp_async16(xd + o, xs + o);
+        unsigned char *sb = base + s * prm.stage_bytes;
+        const bool ok = (uint32_t)srcA < (uint32_t)prm.n_src;
+        const uint32_t okmask = __ballot_sync(0xffffffffu, ok) & (n == 32 ? 0xffffffffu : (1u << n) - 1u);
+        // harmonic rows [e, e+n): one bulk copy of the 16-byte aligned span around
+        // them; a piece past the array's last 16-byte boundary by plain loads
+        const int64_t b0 = (int64_t)ic.e * SHN * 4, b1 = (int64_t)(ic.e + n) * SHN * 4;
+        int64_t a0 = b0, a1 = b1;  // rows of a multiple of 4 floats: the span is aligned already
+        if constexpr (SHN % 4 != 0) {
+            a0 = b0 & ~(int64_t)15;
+            a1 = (b1 + 15) & ~(int64_t)15;
+            if (a1 > sh_bytes_all) a1 = sh_bytes_all & ~(int64_t)15;
+            if (a1 < a0) a1 = a0;
+            if (a1 < b1) {
+                const float *sf = prm.sh + a1 / 4;
+                float *df = reinterpret_cast<float *>(sb + prm.sh_off) + (a1 - a0) / 4;
+                for (int q = lane; q < (int)((b1 - a1) / 4); q += 32) df[q] = sf[q];
             }
-            cp_async_mbar_arrive_noinc(&full[s]);
-        } else if (ok) {
-            bulk_g2s(sb + prm.f_off + lane * FB, xp + (int64_t)srcA * DX, (uint32_t)FB, &full[s], pol_keep);
         }
+        const uint32_t sh_tma = (uint32_t)(a1 - a0);
+        if (okmask != (n == 32 ? 0xffffffffu : (1u << n) - 1u)) {
+            // an edge with an out-of-range source: flag it, and give it a zero row
+            if (lane == 0) set_status(prm.status, TP_DEV_ERR_INDEX);
+            for (int q = 0; q < n; ++q)
+                if (!((okmask >> q) & 1u))
+                    for (int o = lane * 16; o < FB; o += 512)
+                        *reinterpret_cast<uint4 *>(sb + prm.f_off + q * FB + o) = make_uint4(0, 0, 0, 0);
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)n * WB + (uint32_t)__popc(okmask) * FB + sh_tma);
+        __syncwarp();
+        // one copy per lane: lane 0 the weight rows, lane 1 the harmonic span,
+        // lane 2 + q the source row of edge q
+        const int xs = __shfl_up_sync(0xffffffffu, srcA, 2);
+        const int q = lane - 2;
+        const void *gsrc = wb + (int64_t)ic.e * WB;
+        unsigned char *sdst = sb;
+        uint32_t nbytes = (uint32_t)n * WB;
+        uint64_t pol = pol_stream;
+        if (lane == 1) {
+            gsrc = shb_g + a0;
+            sdst = sb + prm.sh_off;
+            nbytes = sh_tma;
+        } else if (lane >= 2) {
+            gsrc = xp + (int64_t)xs * DX;
+            sdst = sb + prm.f_off + q * FB;
+            nbytes = (q < n && ((okmask >> q) & 1u)) ? (uint32_t)FB : 0u;
+            pol = pol_keep;
+        }
+        if (nbytes) bulk_g2s(sdst, gsrc, nbytes, &full[s], pol);
         ++n_issued;
         ic = lc;
         srcA = srcB;
-        lc.e += chunk_n(lc);
-        normalize(lc);
+        lc.e += lc.n;
+        settle(lc);
         srcB = load_src(lc);
     };
     for (int k = 0; k < S; ++k) issue_next();
@@ -408,15 +414,15 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     bool failed = false;
     for (int j = 0; j < np_w && !failed; ++j) {
         const int p = gw + j * nW;
-        const int64_t e_lo = piece_lo(p), e_hi = piece_lo(p + 1);
+        const int e_lo = piece_lo(p), e_hi = piece_lo(p + 1);
         int d_start = __shfl_sync(0xffffffffu, fb, 2 * j);
         int d_end = __shfl_sync(0xffffffffu, fb, 2 * j + 1);
         if (d_start > N) d_start = N;
-        if (d_start > 0 && (int64_t)rp[d_start] > e_lo) d_start -= 1;
+        if (d_start > 0 && rp[d_start] > e_lo) d_start -= 1;
         if (p == nP - 1 || d_end > N) d_end = N;
         if (d_end < d_start) d_end = d_start;
-        const int head_dst = (d_start < d_end && (int64_t)rp[d_start] < e_lo) ? d_start : -1;
-        int tail_dst = (p < nP - 1 && d_end > d_start && (int64_t)rp[d_end] > e_hi) ? d_end - 1 : -1;
+        const int head_dst = (d_start < d_end && rp[d_start] < e_lo) ? d_start : -1;
+        int tail_dst = (p < nP - 1 && d_end > d_start && rp[d_end] > e_hi) ? d_end - 1 : -1;
         if (tail_dst == head_dst) tail_dst = -1;
         if (lane == 0) {
             prm.carry_dst[2 * p] = head_dst;
@@ -425,18 +431,19 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         // row_ptr window: lane l holds rp[wbase + l]
         int wbase = d_start;
         int32_t wv = (wbase + lane <= N) ? rp[wbase + lane] : 0;
-        auto rp_get = [&](int d) -> int64_t {
+        auto rp_get = [&](int d) -> int {
             if (d < wbase || d >= wbase + 32) {
                 wbase = d;
                 wv = (wbase + lane <= N) ? rp[wbase + lane] : 0;
             }
-            return (int64_t)__shfl_sync(0xffffffffu, wv, d - wbase);
+            return __shfl_sync(0xffffffffu, wv, d - wbase);
         };
         int cur_d = d_start;
-        int64_t seg_end = 0;
+        int seg_end = 0;
         auto enter = [&](int d) {
             if (d >= d_end) return;
-            int64_t a = rp_get(d), b = rp_get(d + 1);
+            const int a = rp_get(d);
+            int b = rp_get(d + 1);
             if (a < 0 || b < a || b > E) {
                 if (lane == 0) set_status(prm.status, TP_DEV_ERR_SEGMENT);
                 b = a < 0 ? 0 : (a > E ? E : a);
@@ -457,7 +464,7 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                 for (int c = 0; c < NV; ++c) acc[r][c] = V(0);
         };
         enter(cur_d);
-        int64_t e = e_lo;
+        int e = e_lo;
         while (e < e_hi) {
             const int s = s_done;
             if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph_done))) {
@@ -465,26 +472,27 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                 failed = true;
                 break;
             }
-            const int4 mt = meta[s];
-            const int n = mt.x;
-            const uint32_t vmask = (uint32_t)mt.y;
-            const unsigned char *sb = base + (size_t)s * prm.stage_bytes;
-            const float *shs = reinterpret_cast<const float *>(sb + prm.sh_off) + mt.z;
+            const int n = min(eps, e_hi - e);
+            const unsigned char *sb = base + s * prm.stage_bytes;
+            // M of the chunk's edges (lane-parallel over entries)
+            {
+                const unsigned char *shq = sb + prm.sh_off + (SHN % 4 != 0 ? (e * SHN & 3) * 4 : 0);
+                int4 t[KR];
 #pragma unroll
-            for (int k = 0; k < KR; ++k) {
-                const int r = lane + 32 * k;
-                if (r < P.R) {
-                    const int4 t = tab[r];
-                    const unsigned char *shb = reinterpret_cast<const unsigned char *>(shs);
-                    float *mo = Mw + (LV::kPair ? 2 * r : r);
-                    for (int q = 0; q < n; ++q) {
-                        const float v = fmaf(__int_as_float(t.z), *reinterpret_cast<const float *>(shb + t.x),
-                                             __int_as_float(t.w) * *reinterpret_cast<const float *>(shb + t.y));
-                        if constexpr (LV::kPair) *reinterpret_cast<float2 *>(mo) = make_float2(v, v);
-                        else *mo = v;
-                        shb += SHN * 4;
-                        mo += MS;
+                for (int k = 0; k < KR; ++k) t[k] = (lane + 32 * k < P.R) ? tab[lane + 32 * k] : make_int4(0, 0, 0, 0);
+                float *mo = Mw + (LV::kPair ? 2 * lane : lane);
+                for (int q = 0; q < n; ++q) {
+#pragma unroll
+                    for (int k = 0; k < KR; ++k) {
+                        if (lane + 32 * k < P.R) {
+                            const float v = fmaf(__int_as_float(t[k].z), *reinterpret_cast<const float *>(shq + t[k].x),
+                                                 __int_as_float(t[k].w) * *reinterpret_cast<const float *>(shq + t[k].y));
+                            if constexpr (LV::kPair) *reinterpret_cast<float2 *>(mo + 64 * k) = make_float2(v, v);
+                            else mo[32 * k] = v;
+                        }
                     }
+                    shq += SHN * 4;
+                    mo += MS;
                 }
             }
             __syncwarp();
@@ -496,7 +504,6 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                     ++cur_d;
                     enter(cur_d);
                 }
-                if (!((vmask >> q) & 1u)) continue;
                 const FT *xq = xl + q * (FB / (int)sizeof(FT));
                 V xr[RI][NV];
 #pragma unroll

@@ -166,11 +166,10 @@ struct RingLaunch {
 // for descriptors in the natural layout the kernel is compiled for.
 // Tunables (environment): TPCONV_RING_STAGE_BYTES (target bytes per chunk),
 // TPCONV_RING_STAGES, TPCONV_RING_WARPS (warps per block), TPCONV_RING_ROUNDS
-// (pieces per warp), TPCONV_RING_PACK (packed channel pairs, CPT >= 2),
-// TPCONV_RING_XLSU (gathered rows by cp.async instead of bulk copies).
+// (pieces per warp), TPCONV_RING_PACK (packed channel pairs, CPT >= 2).
 static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin, RingLaunch &rl) {
     const TeamPlan &TP = d->team;
-    if (!TP.valid) return false;
+    if (!TP.valid || E >= (int64_t)1 << 31) return false;  // 32-bit edge indices inside the kernel
     const Tables &T = d->tab;
     const int mul = T.mul;
     if (mul % 32 != 0) return false;
@@ -200,7 +199,7 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int 
     // warp works on the other, and enough warps fit on an SM to keep HBM busy
     const int target = env_int("TPCONV_RING_STAGE_BYTES", 4500);
     int eps = (target + per_edge - 1) / per_edge;
-    eps = eps < 1 ? 1 : (eps > 32 ? 32 : eps);
+    eps = eps < 1 ? 1 : (eps > 30 ? 30 : eps);  // lanes 2..31 issue the gathered rows
     int S = env_int("TPCONV_RING_STAGES", 2);
     S = S < 2 ? 2 : (S > 8 ? 8 : S);
     g.S = S;
@@ -209,11 +208,9 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int 
     g.sh_off = g.f_off + eps * f_bytes;
     g.stage_bytes = round_up(g.sh_off + eps * shn * 4 + 32, 128);  // +32: 16-byte aligned harmonic span
     g.m_off = S * g.stage_bytes;
-    g.meta_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
-    g.bar_off = round_up(g.meta_off + S * 16, 8);
+    g.bar_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
     g.warp_bytes = round_up(g.bar_off + S * 8, 128);
     g.tab_bytes = round_up(16 * TP.R, 128);
-    g.x_lsu = env_int("TPCONV_RING_XLSU", 0) != 0;
     int wpb = env_int("TPCONV_RING_WARPS", 8);
     wpb = wpb < 1 ? 1 : (wpb > kRingMaxWarps ? kRingMaxWarps : wpb);
     while (wpb > 1 && g.tab_bytes + wpb * g.warp_bytes > smem_optin) --wpb;

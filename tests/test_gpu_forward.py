@@ -140,12 +140,11 @@ def test_all_split_kernels(tpc, monkeypatch, irr, dtype, kernel):
 
 RING_GEOMETRIES = {
     "eps1-S2-w1": {"TPCONV_RING_STAGE_BYTES": "1", "TPCONV_RING_STAGES": "2", "TPCONV_RING_WARPS": "1"},
-    "eps32-S2": {"TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_STAGES": "2"},
+    "eps30-S3": {"TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_STAGES": "3"},
     "S8-w8": {"TPCONV_RING_STAGES": "8", "TPCONV_RING_WARPS": "8", "TPCONV_RING_STAGE_BYTES": "4096"},
     "rounds3": {"TPCONV_RING_ROUNDS": "3"},
     "rounds16-eps5": {"TPCONV_RING_ROUNDS": "16", "TPCONV_RING_STAGE_BYTES": "5000"},
-    "xlsu-eps32": {"TPCONV_RING_XLSU": "1", "TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_STAGES": "2"},
-    "xlsu-pack": {"TPCONV_RING_XLSU": "1", "TPCONV_RING_PACK": "1"},
+    "eps30-pack": {"TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_PACK": "1"},
     "nopack": {"TPCONV_RING_PACK": "0"},
 }
 
@@ -154,9 +153,8 @@ RING_GEOMETRIES = {
 @pytest.mark.parametrize("irr,dtype", [(SHAPES[0], torch.float32), (SHAPES[1], torch.float32),
                                        (SHAPES[2], torch.bfloat16)], ids=["cpt1", "cpt4", "cpt2-bf16"])
 def test_ring_geometries(tpc, monkeypatch, irr, dtype, geo):
-    """The warp ring with chunks of 1 to 32 edges, 2 to 8 stages, 1 to 8 warps
-    per block, several pieces per warp, gathered rows by bulk copies or by
-    cp.async, packed or scalar FMAs, on a graph with a 1000-edge
+    """The warp ring with chunks of 1 to 30 edges, 2 to 8 stages, 1 to 8 warps
+    per block, several pieces per warp, packed or scalar FMAs, on a graph with a 1000-edge
     destination (cut across many pieces), empty destinations and a ragged tail."""
     for k, v in RING_GEOMETRIES[geo].items():
         monkeypatch.setenv(k, v)
