@@ -3,12 +3,13 @@
 
 namespace tpc {
 
-// cpt: channels per lane (mul = 32 * cpt); pk: packed channel pairs. The
-// register caps (blocks of 256 threads per SM) keep one channel per lane at 3
-// blocks per SM and packed pairs of two channels at 2.
+// cpt: channels per lane (mul = 32 * cpt); pk: packed channel (cpt >= 2) or
+// edge (cpt == 1) pairs. The register caps (blocks of 256 threads per SM) keep
+// one channel per lane at 3 blocks per SM and packed pairs at 2.
 const void *ring_kernel_f32(int shape, int cpt, int pk) {
 #define TPC_R(SI, LI, LSH, LO) \
-    if (shape == SI && cpt == 1) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 1, false, 3, float>); \
+    if (shape == SI && cpt == 1 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 1, false, 3, float>); \
+    if (shape == SI && cpt == 1 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 1, true, 2, float>); \
     if (shape == SI && cpt == 2 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 2, false, 1, float>); \
     if (shape == SI && cpt == 2 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 2, true, 2, float>); \
     if (shape == SI && cpt == 4 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 4, false, 1, float>); \

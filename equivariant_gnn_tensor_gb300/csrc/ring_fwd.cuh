@@ -89,11 +89,28 @@ __device__ __forceinline__ f32x2 pack2(float lo, float hi) {
     asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
     return d;
 }
+__device__ __forceinline__ float lo_f(f32x2 v) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+    return a;
+}
+__device__ __forceinline__ float hi_f(f32x2 v) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+    return b;
+}
+__device__ __forceinline__ float to_float(float v) { return v; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// PK with CPT >= 2: a lane value is two neighbouring channels of one edge.
+// PK with CPT == 1 ("edge pairs"): a lane value is one channel of two
+// consecutive edges of the same destination, whose partial sums are kept
+// apart and added when the destination is stored.
 template <int CPT, bool PK>
 struct LaneVec {
-    static constexpr bool kPair = PK && CPT >= 2;
-    static constexpr int NV = kPair ? CPT / 2 : CPT;
+    static constexpr bool kPair = PK;
+    static constexpr bool kEdgePair = PK && CPT == 1;
+    static constexpr int NV = kPair ? (kEdgePair ? 1 : CPT / 2) : CPT;
     using V = typename std::conditional<kPair, f32x2, float>::type;
 };
 
@@ -172,12 +189,15 @@ constexpr int entry_at(int T, int pos) {
 }
 
 // One program path for one edge: acc[lc-block row k] += w_T * sum_i M_T[i][k] x[la-block row i].
-// wl: this lane's channels of the edge's weight row; Mq: the edge's M (entries
-// duplicated into pairs when packed).
+// wl: this lane's channels of the edge's weight row (wlB: of the second edge,
+// edge pairs only); Mq: the edge's M (entries duplicated into pairs for channel
+// pairs, the two edges' entries interleaved for edge pairs); use_a / use_b:
+// edge pairs only, whether each edge takes part (an absent one adds zero).
 template <int LI, int LSH, int LO, int T, int CPT, bool PK, typename FT>
 __device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[rows_upto(LO)][LaneVec<CPT, PK>::NV],
                                           const typename LaneVec<CPT, PK>::V (&xr)[rows_upto(LI)][LaneVec<CPT, PK>::NV],
-                                          const FT *wl, const float *Mq) {
+                                          const FT *wl, const FT *wlB, const float *Mq, bool use_a = true,
+                                          bool use_b = true) {
     using LV = LaneVec<CPT, PK>;
     constexpr int MUL = 32 * CPT;
     using V = typename LV::V;
@@ -186,7 +206,12 @@ __device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[ro
     constexpr int LA = P.p[T].la, LC = P.p[T].lc;
     constexpr int NA = 2 * LA + 1, NC = 2 * LC + 1, NZ = P.nz[T], MO = P.moff[T];
     V wv[NV];
-    load_lane<CPT, PK>(wl + T * MUL, wv);
+    if constexpr (LV::kEdgePair) {
+        const float a = to_float(wl[T * MUL]), b = to_float(wlB[T * MUL]);
+        wv[0] = pack2(use_a ? a : 0.f, use_b ? b : 0.f);
+    } else {
+        load_lane<CPT, PK>(wl + T * MUL, wv);
+    }
     // M entries of this path: 4 per 16-byte load (singles) or 2 (pairs)
     constexpr int PER = LV::kPair ? 2 : 4;
     constexpr int NL = (NZ + PER - 1) / PER;
@@ -248,7 +273,8 @@ __device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[ro
 
 template <int CPT, bool PK>
 __device__ __forceinline__ void store_lane(float *p, const typename LaneVec<CPT, PK>::V (&v)[LaneVec<CPT, PK>::NV]) {
-    if constexpr (!LaneVec<CPT, PK>::kPair) store_vec<CPT>(p, v);
+    if constexpr (LaneVec<CPT, PK>::kEdgePair) *p = lo_f(v[0]) + hi_f(v[0]);
+    else if constexpr (!LaneVec<CPT, PK>::kPair) store_vec<CPT>(p, v);
     else if constexpr (CPT == 4) *reinterpret_cast<ulonglong2 *>(p) = make_ulonglong2(v[0], v[1]);
     else *reinterpret_cast<f32x2 *>(p) = v[0];
 }
@@ -288,6 +314,8 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     if (lane == 0)
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
+    if constexpr (LV::kEdgePair)  // an absent second edge reads finite (zero) M entries
+        for (int i = lane; i < eps * MS; i += 32) Mw[i] = 0.f;
     __syncwarp();
 
     const int nP = prm.n_pieces, nW = prm.n_warps, N = prm.n_dst;
@@ -402,6 +430,23 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     } else if (lane < 2 * np_w) {
         fb = lane_first_geq(rp, N, piece_lo(gw + (lane >> 1) * nW + (lane & 1)));
     }
+    // and row_ptr there, so a piece starts without a dependent load
+    const int rb = lane < 2 * np_w ? rp[min(fb, N)] : 0;
+    auto piece_dstart = [&](int j) {  // first destination of piece j and whether it began earlier
+        const int e_lo = piece_lo(gw + j * nW);
+        int d = min(__shfl_sync(0xffffffffu, fb, 2 * j), N);
+        const bool earlier = d > 0 && __shfl_sync(0xffffffffu, rb, 2 * j) > e_lo;
+        return earlier ? -(d - 1) - 1 : d;  // negative: d-1 started in an earlier piece
+    };
+    // row_ptr window of the next piece, loaded one piece ahead
+    int wv_next = 0, wbase_next = -1;
+    auto prefetch_window = [&](int j) {
+        if (j >= np_w) return;
+        const int ds = piece_dstart(j);
+        wbase_next = ds < 0 ? -ds - 1 : ds;
+        wv_next = (wbase_next + lane <= N) ? rp[wbase_next + lane] : 0;
+    };
+    prefetch_window(0);
 
     // ---- consume side ---------------------------------------------------------------
     V acc[RO][NV];
@@ -415,22 +460,24 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     for (int j = 0; j < np_w && !failed; ++j) {
         const int p = gw + j * nW;
         const int e_lo = piece_lo(p), e_hi = piece_lo(p + 1);
-        int d_start = __shfl_sync(0xffffffffu, fb, 2 * j);
+        const int ds = piece_dstart(j);
+        const int d_start = ds < 0 ? -ds - 1 : ds;
         int d_end = __shfl_sync(0xffffffffu, fb, 2 * j + 1);
-        if (d_start > N) d_start = N;
-        if (d_start > 0 && rp[d_start] > e_lo) d_start -= 1;
+        const int rp_end = __shfl_sync(0xffffffffu, rb, 2 * j + 1);  // row_ptr[min(d_end, N)]
         if (p == nP - 1 || d_end > N) d_end = N;
         if (d_end < d_start) d_end = d_start;
-        const int head_dst = (d_start < d_end && rp[d_start] < e_lo) ? d_start : -1;
-        int tail_dst = (p < nP - 1 && d_end > d_start && rp[d_end] > e_hi) ? d_end - 1 : -1;
+        // d_start began in an earlier piece: a head partial; d_end - 1 runs on past e_hi: a tail partial
+        const int head_dst = (ds < 0 && d_start < d_end) ? d_start : -1;
+        int tail_dst = (p < nP - 1 && d_end > d_start && rp_end > e_hi) ? d_end - 1 : -1;
         if (tail_dst == head_dst) tail_dst = -1;
         if (lane == 0) {
             prm.carry_dst[2 * p] = head_dst;
             prm.carry_dst[2 * p + 1] = tail_dst;
         }
         // row_ptr window: lane l holds rp[wbase + l]
-        int wbase = d_start;
-        int32_t wv = (wbase + lane <= N) ? rp[wbase + lane] : 0;
+        int wbase = wbase_next;
+        int32_t wv = wv_next;
+        prefetch_window(j + 1);
         auto rp_get = [&](int d) -> int {
             if (d < wbase || d >= wbase + 32) {
                 wbase = d;
@@ -487,32 +534,78 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                         if (lane + 32 * k < P.R) {
                             const float v = fmaf(__int_as_float(t[k].z), *reinterpret_cast<const float *>(shq + t[k].x),
                                                  __int_as_float(t[k].w) * *reinterpret_cast<const float *>(shq + t[k].y));
-                            if constexpr (LV::kPair) *reinterpret_cast<float2 *>(mo + 64 * k) = make_float2(v, v);
+                            if constexpr (LV::kEdgePair) mo[64 * k + (q & 1)] = v;
+                            else if constexpr (LV::kPair) *reinterpret_cast<float2 *>(mo + 64 * k) = make_float2(v, v);
                             else mo[32 * k] = v;
                         }
                     }
                     shq += SHN * 4;
-                    mo += MS;
+                    if (!LV::kEdgePair || (q & 1)) mo += MS;  // edge pairs: one block per two edges
                 }
             }
             __syncwarp();
             const FT *wl = reinterpret_cast<const FT *>(sb) + ch0;
             const FT *xl = reinterpret_cast<const FT *>(sb + prm.f_off) + ch0;
-            for (int q = 0; q < n; ++q, ++e) {
-                while (e >= seg_end && cur_d < d_end) {
-                    store_row(cur_d);
-                    ++cur_d;
-                    enter(cur_d);
-                }
-                const FT *xq = xl + q * (FB / (int)sizeof(FT));
-                V xr[RI][NV];
+            if constexpr (LV::kEdgePair) {
+                // edges (q, q+1) of an aligned pair together when they share the
+                // destination, else one at a time with the other half zeroed
+                for (int q = 0; q < n; q += 2) {
+                    while (e >= seg_end && cur_d < d_end) {
+                        store_row(cur_d);
+                        ++cur_d;
+                        enter(cur_d);
+                    }
+                    const float *Mq = Mw + (q >> 1) * MS;
+                    const FT *xa = xl + q * (FB / (int)sizeof(FT)), *wa = wl + q * (WB / (int)sizeof(FT));
+                    // the second slot only when it holds an edge of this chunk
+                    const bool has_b = q + 1 < n;
+                    const FT *xb = has_b ? xa + FB / (int)sizeof(FT) : xa;
+                    const FT *wb2 = has_b ? wa + WB / (int)sizeof(FT) : wa;
+                    auto run = [&](bool use_a, bool use_b) {
+                        V xr[RI][1];
 #pragma unroll
-                for (int r = 0; r < RI; ++r) load_lane<CPT, PK>(xq + r * MUL, xr[r]);
-                const FT *wq = wl + q * (WB / (int)sizeof(FT));
-                const float *Mq = Mw + q * MS;
-                static_for<P.n>([&](auto tc) {
-                    ring_path<LI, LSH, LO, decltype(tc)::value, CPT, PK, FT>(acc, xr, wq, Mq);
-                });
+                        for (int r = 0; r < RI; ++r) {
+                            const float a = to_float(xa[r * MUL]), b = to_float(xb[r * MUL]);
+                            xr[r][0] = pack2(use_a ? a : 0.f, use_b ? b : 0.f);
+                        }
+                        static_for<P.n>([&](auto tc) {
+                            ring_path<LI, LSH, LO, decltype(tc)::value, CPT, PK, FT>(acc, xr, wa, wb2, Mq, use_a, use_b);
+                        });
+                    };
+                    if (has_b && e + 1 < seg_end) {
+                        run(true, true);
+                        e += 2;
+                    } else {
+                        run(true, false);
+                        ++e;
+                        if (has_b) {
+                            while (e >= seg_end && cur_d < d_end) {
+                                store_row(cur_d);
+                                ++cur_d;
+                                enter(cur_d);
+                            }
+                            run(false, true);
+                            ++e;
+                        }
+                    }
+                }
+            } else {
+                for (int q = 0; q < n; ++q, ++e) {
+                    while (e >= seg_end && cur_d < d_end) {
+                        store_row(cur_d);
+                        ++cur_d;
+                        enter(cur_d);
+                    }
+                    const FT *xq = xl + q * (FB / (int)sizeof(FT));
+                    V xr[RI][NV];
+#pragma unroll
+                    for (int r = 0; r < RI; ++r) load_lane<CPT, PK>(xq + r * MUL, xr[r]);
+                    const FT *wq = wl + q * (WB / (int)sizeof(FT));
+                    const float *Mq = Mw + q * MS;
+                    static_for<P.n>([&](auto tc) {
+                        ring_path<LI, LSH, LO, decltype(tc)::value, CPT, PK, FT>(acc, xr, wq, wq, Mq);
+                    });
+                }
             }
             // this warp's reads of the stage come before the bulk copies that refill it
             fence_proxy_async_smem();

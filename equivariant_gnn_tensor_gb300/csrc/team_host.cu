@@ -166,7 +166,7 @@ struct RingLaunch {
 // for descriptors in the natural layout the kernel is compiled for.
 // Tunables (environment): TPCONV_RING_STAGE_BYTES (target bytes per chunk),
 // TPCONV_RING_STAGES, TPCONV_RING_WARPS (warps per block), TPCONV_RING_ROUNDS
-// (pieces per warp), TPCONV_RING_PACK (packed channel pairs, CPT >= 2).
+// (pieces per warp), TPCONV_RING_PACK (packed FMAs over channel or edge pairs).
 static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin, RingLaunch &rl) {
     const TeamPlan &TP = d->team;
     if (!TP.valid || E >= (int64_t)1 << 31) return false;  // 32-bit edge indices inside the kernel
@@ -175,7 +175,10 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int 
     if (mul % 32 != 0) return false;
     const int cpt = mul / 32;
     if (cpt != 1 && cpt != 2 && cpt != 4) return false;
-    const int pk = cpt >= 2 ? env_int("TPCONV_RING_PACK", cpt == 2 ? 1 : 0) != 0 : 0;
+    // packed FMAs: channel pairs for two channels per lane, edge pairs for one
+    // (the two smaller programs; the larger ones run out of registers); four
+    // channels per lane keep plain FMAs (shorter dependent latency)
+    const int pk = env_int("TPCONV_RING_PACK", cpt == 4 ? 0 : (cpt == 2 || TP.shape <= 1)) != 0;
     // natural layout: block l at l*l*mul, paths in program order
     const ProgShape shp = kProgShapes[TP.shape];
     const Program prog = make_natural_program(shp.li, shp.lsh, shp.lo);

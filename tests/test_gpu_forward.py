@@ -146,6 +146,7 @@ RING_GEOMETRIES = {
     "rounds16-eps5": {"TPCONV_RING_ROUNDS": "16", "TPCONV_RING_STAGE_BYTES": "5000"},
     "eps30-pack": {"TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_PACK": "1"},
     "nopack": {"TPCONV_RING_PACK": "0"},
+    "rounds4-S4": {"TPCONV_RING_ROUNDS": "4", "TPCONV_RING_STAGES": "4"},
 }
 
 
