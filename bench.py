@@ -195,7 +195,7 @@ def cpu_baseline(wl, host, n, target_s: float):
     row_ptr = np.zeros(n + 1, dtype=np.int64)
     np.cumsum(np.bincount(dst, minlength=n), out=row_ptr[1:])
 
-    def run(rows):
+    def run(rows, reps=1):
         sel = np.concatenate([order[row_ptr[r]:row_ptr[r + 1]] for r in rows]) if len(rows) else np.zeros(0, int)
         lrp = np.zeros(len(rows) + 1, dtype=np.int64)
         np.cumsum([row_ptr[r + 1] - row_ptr[r] for r in rows], out=lrp[1:])
@@ -203,7 +203,8 @@ def cpu_baseline(wl, host, n, target_s: float):
         xs = x.astype(np.float64)
         ws = w[sel].astype(np.float64)
         t0 = time.perf_counter()
-        cref.conv_forward(plan, xs, sh, ws, src[sel], lrp, len(rows), threads=cores)
+        for _ in range(reps):
+            cref.conv_forward(plan, xs, sh, ws, src[sel], lrp, len(rows), threads=cores)
         return time.perf_counter() - t0, len(sel)
 
     rows = np.arange(min(n, 32))
@@ -212,7 +213,12 @@ def cpu_baseline(wl, host, n, target_s: float):
     k = int(min(n, max(32, len(rows) * scale)))
     rows = np.arange(k)
     dt, ne = run(rows)
-    return ne / dt, cores, f"first {k} destination rows ({ne} edges) of the workload, fp64 oracle, {dt:.1f} s"
+    reps = 1
+    if k == n and dt < 0.5 * target_s:      # the whole workload is quick: repeat it
+        reps = int(min(200, max(1, target_s / max(dt, 1e-3))))
+        dt, ne = run(rows, reps)
+    what = f"first {k} destination rows" if k < n else f"all {n} destination rows"
+    return ne * reps / dt, cores, f"{what} ({ne} edges) x {reps} of the workload, fp64 oracle, {dt:.1f} s"
 
 
 def bench_reference(args):

@@ -409,6 +409,9 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             pol = pol_keep;
         }
         if (nbytes) bulk_g2s(sdst, gsrc, nbytes, &full[s], pol);
+        // the source indices a few chunks on start their way to L2 now, so the
+        // register load two chunks ahead does not wait on HBM
+        if (lane == 0 && ic.e + 16 * eps < E) asm volatile("prefetch.global.L2 [%0];" ::"l"(srcp + ic.e + 16 * eps));
         ++n_issued;
         ic = lc;
         srcA = srcB;
