@@ -18,8 +18,8 @@ cudaError_t csr_build_launch(const int32_t *keys, int64_t E, int32_t N, int32_t 
 cudaError_t sh_launch(const float *vec, int64_t E, int normalize, const Tables &T, float *sh, cudaStream_t stream);
 int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
-size_t team_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin);
-cudaError_t team_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
+size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin);
+cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
                          const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
                          float *out, void *ws, size_t ws_bytes, int sms, int smem_optin, int *status,
                          cudaStream_t stream);
@@ -179,7 +179,7 @@ extern "C" tp_status tp_conv_forward_workspace_size(const tp_desc *desc, tp_dtyp
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
-    *bytes = team_workspace_bytes(desc, dtype, E, dev.sms, dev.smem_optin);
+    *bytes = split_workspace_bytes(desc, dtype, E, dev.sms, dev.smem_optin);
     return TP_OK;
 }
 
@@ -203,7 +203,7 @@ extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
         DevInfo dev;
         tp_status st = dev_info(dev);
         if (st != TP_OK) return st;
-        const cudaError_t e = team_forward(desc, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, workspace,
+        const cudaError_t e = split_forward(desc, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, workspace,
                                            workspace_bytes, dev.sms, dev.smem_optin, dev.status,
                                            static_cast<cudaStream_t>(stream));
         if (e == cudaSuccess) return TP_OK;

@@ -168,9 +168,9 @@ void real_cg(int l1, int l2, int l3, double *C) {
 
 // Match the descriptor against the compiled path programs (program.h) and
 // build the program-layout recipe for the first one that fits.
-void plan_team(tp_desc *d) {
+void plan_program(tp_desc *d) {
     using namespace tpc;
-    TeamPlan &TP = d->team;
+    ProgramPlan &TP = d->prog;
     TP.valid = 0;
     for (int si = 0; si < kNumProgShapes; ++si) {
         const ProgShape sh = kProgShapes[si];
@@ -373,7 +373,7 @@ extern "C" tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh
         for (auto &e : col[j]) { T.tr_r[t] = (uint16_t)e.first; T.tr_c[t] = e.second; ++t; }
     }
     T.tr_ptr[dim_sh] = (uint16_t)t;
-    plan_team(d);
+    plan_program(d);
     *out = d;
     return TP_OK;
 }

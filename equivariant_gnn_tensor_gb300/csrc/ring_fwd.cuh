@@ -33,9 +33,53 @@
 //            carry_fixup_kernel adds in piece order. No atomics: results are
 //            bitwise reproducible for a given launch geometry.
 #pragma once
-#include "team_fwd.cuh"
+#include <type_traits>
+#include <utility>
+
+#include "common.cuh"
+#include "conv_common.cuh"
+#include "program.h"
 
 namespace tpc {
+
+template <int N, class F, int... I>
+__device__ __forceinline__ void static_for_impl(F &&f, std::integer_sequence<int, I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, class F>
+__device__ __forceinline__ void static_for(F &&f) {
+    static_for_impl<N>(f, std::make_integer_sequence<int, N>{});
+}
+
+// Smallest d in [0, N] with rp[d] >= target (N+1 if none); 32-way search by a
+// whole warp. rp must be non-decreasing for a meaningful answer; every access
+// stays inside rp[0..N] regardless.
+__device__ __forceinline__ int warp_first_geq(const int32_t *rp, int N, int64_t target, int lane) {
+    int lo = 0, hi = N + 1;  // answer in [lo, hi]; position hi is known true (or N+1)
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) / 32;
+        const int q = lo + lane * step;
+        const bool pr = q >= hi || q > N || (int64_t)rp[q] >= target;
+        const uint32_t m = __ballot_sync(0xffffffffu, pr);
+        if (m == 0) {
+            lo = lo + 31 * step + 1;
+        } else {
+            const int k = __ffs(m) - 1;
+            const int nhi = lo + k * step;
+            lo = k == 0 ? lo : lo + (k - 1) * step + 1;
+            hi = nhi;
+        }
+    }
+    const int q = lo + lane;
+    const bool pr = q >= hi || q > N || (int64_t)rp[q] >= target;
+    const uint32_t m = __ballot_sync(0xffffffffu, pr);
+    return m ? lo + __ffs(m) - 1 : hi;
+}
+
+// out[d] = tail partial of the piece where d starts + head partials of the
+// following pieces that continue d, added in piece order. One warp per piece.
+__global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_t *__restrict__ carry_dst, int n_pieces,
+                                   int dim_out, float *__restrict__ out);
 
 constexpr int kRingMaxWarps = 8;
 constexpr int kRingMaxPiecesPerWarp = 16;
@@ -89,16 +133,8 @@ __device__ __forceinline__ f32x2 pack2(float lo, float hi) {
     asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
     return d;
 }
-__device__ __forceinline__ float lo_f(f32x2 v) {
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-    return a;
-}
-__device__ __forceinline__ float hi_f(f32x2 v) {
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-    return b;
-}
+__device__ __forceinline__ float lo_f(f32x2 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ float to_float(float v) { return v; }
 __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 

@@ -1,0 +1,190 @@
+// Host side of the program-specialised forward: launch geometry of the warp
+// ring kernel, the workspace for head/tail partial rows of destinations cut by
+// piece boundaries, and the partial-merging kernel.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+
+#include "ring_fwd.cuh"
+
+namespace tpc {
+
+const void *ring_kernel_f32(int shape, int cpt, int pk);
+const void *ring_kernel_bf16(int shape, int cpt, int pk);
+
+__global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_t *__restrict__ carry_dst,
+                                   int n_pieces, int dim_out, float *__restrict__ out) {
+    const int c = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (c >= n_pieces) return;
+    const int d = carry_dst[2 * c + 1];
+    if (d < 0) return;
+    for (int col = lane * 4; col < dim_out; col += 128) {
+        float4 v = *reinterpret_cast<const float4 *>(carry + (int64_t)(2 * c + 1) * dim_out + col);
+        for (int c2 = c + 1; c2 < n_pieces && carry_dst[2 * c2] == d; ++c2) {
+            const float4 u = *reinterpret_cast<const float4 *>(carry + (int64_t)(2 * c2) * dim_out + col);
+            v.x += u.x;
+            v.y += u.y;
+            v.z += u.z;
+            v.w += u.w;
+        }
+        *reinterpret_cast<float4 *>(out + (int64_t)d * dim_out + col) = v;
+    }
+}
+
+static int env_int(const char *name, int dflt) {
+    const char *v = std::getenv(name);
+    return v && *v ? std::atoi(v) : dflt;
+}
+
+static size_t carry_bytes(int streams, int dim_out) {
+    const size_t a = (size_t)2 * streams * dim_out * sizeof(float);
+    return (a + 255) / 256 * 256 + (size_t)2 * streams * sizeof(int32_t);
+}
+
+struct RingLaunch {
+    const void *fn = nullptr;
+    RingParams geo{};  // layout fields only
+    int wpb = 0, n_warps = 0, n_pieces = 0, smem = 0;
+};
+
+// One warp covers all channels, CPT = mul/32 in {1,2,4} channels per lane,
+// for descriptors in the natural layout the kernel is compiled for.
+// Tunables (environment): TPCONV_RING_STAGE_BYTES (target bytes per chunk),
+// TPCONV_RING_STAGES, TPCONV_RING_WARPS (warps per block), TPCONV_RING_ROUNDS
+// (pieces per warp), TPCONV_RING_PACK (packed FMAs over channel or edge pairs).
+static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin, RingLaunch &rl) {
+    const ProgramPlan &TP = d->prog;
+    if (!TP.valid || E >= (int64_t)1 << 31) return false;  // 32-bit edge indices inside the kernel
+    const Tables &T = d->tab;
+    const int mul = T.mul;
+    if (mul % 32 != 0) return false;
+    const int cpt = mul / 32;
+    if (cpt != 1 && cpt != 2 && cpt != 4) return false;
+    // packed FMAs: channel pairs for two channels per lane, edge pairs for one
+    // (the two smaller programs; the larger ones run out of registers); four
+    // channels per lane keep plain FMAs (shorter dependent latency)
+    const int pk = env_int("TPCONV_RING_PACK", cpt == 4 ? 0 : (cpt == 2 || TP.shape <= 1)) != 0;
+    // natural layout: block l at l*l*mul, paths in program order
+    const ProgShape shp = kProgShapes[TP.shape];
+    const Program prog = make_natural_program(shp.li, shp.lsh, shp.lo);
+    if (T.dim_x != (shp.li + 1) * (shp.li + 1) * mul || T.dim_out != (shp.lo + 1) * (shp.lo + 1) * mul ||
+        T.dim_sh != (shp.lsh + 1) * (shp.lsh + 1) || T.wnum != prog.n * mul || TP.R != prog.R)
+        return false;
+    for (int l = 0; l <= shp.li; ++l)
+        if (T.x_off[l] != l * l * mul) return false;
+    for (int l = 0; l <= shp.lo; ++l)
+        if (T.o_off[l] != l * l * mul) return false;
+    for (int t = 0; t < prog.n; ++t)
+        if (TP.wofs[t] != t * mul) return false;
+    rl.fn = dtype == TP_F32 ? ring_kernel_f32(TP.shape, cpt, pk) : ring_kernel_bf16(TP.shape, cpt, pk);
+    if (!rl.fn) return false;
+    const int esz = dtype == TP_F32 ? 4 : 2;
+    RingParams &g = rl.geo;
+    const int w_bytes = T.wnum * esz, f_bytes = T.dim_x * esz;
+    const int shn = T.dim_sh;
+    const int per_edge = w_bytes + f_bytes + shn * 4;
+    // about 4.5 KB per chunk and two stages per warp: one chunk lands while the
+    // warp works on the other, and enough warps fit on an SM to keep HBM busy
+    const int target = env_int("TPCONV_RING_STAGE_BYTES", 4500);
+    int eps = (target + per_edge - 1) / per_edge;
+    eps = eps < 1 ? 1 : (eps > 30 ? 30 : eps);  // lanes 2..31 issue the gathered rows
+    int S = env_int("TPCONV_RING_STAGES", 2);
+    S = S < 2 ? 2 : (S > 8 ? 8 : S);
+    g.S = S;
+    g.eps = eps;
+    g.f_off = eps * w_bytes;
+    g.sh_off = g.f_off + eps * f_bytes;
+    g.stage_bytes = round_up(g.sh_off + eps * shn * 4 + 32, 128);  // +32: 16-byte aligned harmonic span
+    g.m_off = S * g.stage_bytes;
+    g.bar_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
+    g.warp_bytes = round_up(g.bar_off + S * 8, 128);
+    g.tab_bytes = round_up(16 * TP.R, 128);
+    int wpb = env_int("TPCONV_RING_WARPS", 8);
+    wpb = wpb < 1 ? 1 : (wpb > kRingMaxWarps ? kRingMaxWarps : wpb);
+    while (wpb > 1 && g.tab_bytes + wpb * g.warp_bytes > smem_optin) --wpb;
+    rl.smem = g.tab_bytes + wpb * g.warp_bytes;
+    if (rl.smem > smem_optin) return false;
+    rl.wpb = wpb;
+    if (cudaFuncSetAttribute(rl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess) return false;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rl.fn, 32 * wpb, rl.smem) != cudaSuccess || occ < 1)
+        return false;
+    long long nw = (long long)sms * occ * wpb;
+    const long long by_edges = (E + 63) / 64;  // at least ~64 edges per warp
+    if (nw > by_edges) nw = by_edges;
+    if (nw < 1) nw = 1;
+    int rounds = env_int("TPCONV_RING_ROUNDS", 1);
+    rounds = rounds < 1 ? 1 : (rounds > kRingMaxPiecesPerWarp ? kRingMaxPiecesPerWarp : rounds);
+    rl.n_warps = (int)nw;
+    rl.n_pieces = (int)nw * rounds;
+    return true;
+}
+
+static cudaError_t ring_forward(const tp_desc *d, const RingLaunch &rl0, const void *x, const float *sh,
+                                const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src,
+                                int32_t N_dst, int64_t E, float *out, void *ws, size_t ws_bytes, int *status,
+                                cudaStream_t stream) {
+    RingLaunch rl = rl0;
+    const Tables &T = d->tab;
+    const int rounds = rl.n_pieces / rl.n_warps;
+    // a smaller caller workspace: fewer warps
+    while (rl.n_warps > 1 && carry_bytes(rl.n_warps * rounds, T.dim_out) > ws_bytes) rl.n_warps = (rl.n_warps + 1) / 2;
+    rl.n_pieces = rl.n_warps * rounds;
+    if (!ws || carry_bytes(rl.n_pieces, T.dim_out) > ws_bytes) return cudaErrorNotSupported;
+    static_assert(sizeof(RingParams) < 32000, "kernel parameter block too large");
+    RingParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm = rl.geo;
+    std::memcpy(prm.ej, d->prog.ej, sizeof(uint32_t) * d->prog.R);
+    std::memcpy(prm.ec, d->prog.ec, sizeof(float) * 2 * d->prog.R);
+    prm.x = x;
+    prm.sh = sh;
+    prm.w = w;
+    prm.src = src;
+    prm.row_ptr = row_ptr;
+    prm.out = out;
+    prm.carry = static_cast<float *>(ws);
+    const size_t cb = ((size_t)2 * rl.n_pieces * T.dim_out * sizeof(float) + 255) / 256 * 256;
+    prm.carry_dst = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(ws) + cb);
+    prm.status = status;
+    prm.n_src = N_src;
+    prm.n_dst = N_dst;
+    prm.n_warps = rl.n_warps;
+    prm.n_pieces = rl.n_pieces;
+    prm.E = E;
+    const int blocks = (rl.n_warps + rl.wpb - 1) / rl.wpb;
+    void *args[] = {&prm};
+    cudaError_t e = cudaLaunchKernel(rl.fn, dim3(blocks), dim3(32 * rl.wpb), args, (size_t)rl.smem, stream);
+    if (e != cudaSuccess) return e;
+    const int wpb = 8;
+    carry_fixup_kernel<<<(rl.n_pieces + wpb - 1) / wpb, 32 * wpb, 0, stream>>>(prm.carry, prm.carry_dst, rl.n_pieces,
+                                                                                T.dim_out, out);
+    return cudaGetLastError();
+}
+
+// Workspace the split forward needs (0: this descriptor has no program kernel
+// or the input does not qualify).
+size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin) {
+    RingLaunch rl;
+    if (!ring_plan(d, dtype, E, sms, smem_optin, rl)) return 0;
+    return carry_bytes(rl.n_pieces, d->tab.dim_out);
+}
+
+// Launches the ring kernel (+ partial merge). Returns cudaErrorNotSupported
+// when the descriptor or the pointers do not qualify, or the workspace cannot
+// hold the partials (the caller then uses the generic kernel).
+cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
+                          const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
+                          float *out, void *ws, size_t ws_bytes, int sms, int smem_optin, int *status,
+                          cudaStream_t stream) {
+    if (env_int("TPCONV_DISABLE_SPLIT", 0)) return cudaErrorNotSupported;
+    RingLaunch rl;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
+                         reinterpret_cast<uintptr_t>(sh);
+    if ((al & 15u) != 0 || !ring_plan(d, dtype, E, sms, smem_optin, rl)) return cudaErrorNotSupported;
+    return ring_forward(d, rl, x, sh, w, src, row_ptr, N_src, N_dst, E, out, ws, ws_bytes, status, stream);
+}
+
+}  // namespace tpc

@@ -44,7 +44,7 @@ struct Tables {
 // Runtime tables for a compile-time path program (program.h): valid when the
 // descriptor's paths are exactly the program's and every nonzero
 // Clebsch-Gordan entry lies inside the program's M pattern.
-struct TeamPlan {
+struct ProgramPlan {
     int32_t valid;
     int32_t shape;   // index into kProgShapes
     int32_t R, nnz;
@@ -68,5 +68,5 @@ struct tp_desc {
     int path_a[tpc::kMaxPaths], path_b[tpc::kMaxPaths], path_c[tpc::kMaxPaths];
     double *cg[tpc::kMaxPaths];  // dense [2la+1][2lb+1][2lc+1]
     tpc::Tables tab;
-    tpc::TeamPlan team;
+    tpc::ProgramPlan prog;
 };

@@ -116,22 +116,11 @@ def test_bipartite_sources(tpc):
     assert err(out, oracle_forward(prob)) <= FP32_TOL
 
 
-KERNELS = {
-    "warp-ring": {},                                                        # default
-    "warp-cpasync": {"TPCONV_FWD_KERNEL": "direct", "TPCONV_FWD_PIPELINED": "0"},
-    "cta-pipeline": {"TPCONV_FWD_KERNEL": "team", "TPCONV_FWD_PIPELINED": "1"},
-}
-
-
-@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("irr,dtype", [(SHAPES[0], torch.float32), (SHAPES[1], torch.float32),
                                        (SHAPES[2], torch.bfloat16), (SHAPES[3], torch.float32)],
                          ids=["tiny", "medium", "large-bf16", "lesson"])
-def test_all_split_kernels(tpc, monkeypatch, irr, dtype, kernel):
-    """Every edge-balanced kernel (the warp-private TMA ring, the warp-private
-    cp.async ring and the CTA pipeline with a producer warp) against the oracle."""
-    for k, v in KERNELS[kernel].items():
-        monkeypatch.setenv(k, v)
+def test_split_kernel_default_geometry(tpc, irr, dtype):
+    """The warp-ring kernel in its default launch geometry against the oracle."""
     prob = make_problem(*irr, n_src=400, n_dst=333, E=9000, seed=14)
     out, _, _ = run(tpc, prob, dtype)
     assert err(out, oracle_forward(prob, dtype)) <= FP32_TOL
