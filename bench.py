@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward timing (medium only)")
     return ap.parse_args()
 
 
@@ -182,6 +183,48 @@ def algorithmic_bytes(desc, n, E, esz):
     out, row pointers."""
     return (E * desc.weight_numel * esz + E * desc.dim_sh * 4 + E * 4 + n * desc.dim_x * esz
             + n * desc.dim_out * 4 + (n + 1) * 4)
+
+
+def backward_bytes(desc, n, E):
+    """Compulsory bytes of one fp32 backward: w read and dw written, sh read and
+    dsh written, src and the source permutation, x and grad_out read, dx
+    written, both row-pointer arrays."""
+    return (2 * E * desc.weight_numel * 4 + 2 * E * desc.dim_sh * 4 + 2 * E * 4 + 3 * n * desc.dim_x * 4
+            + 2 * (n + 1) * 4)
+
+
+def time_backward(desc, inp, n, E, out, ws, stream, tpc, torch, steps: int = 200):
+    """Backward (dx, dw, dsh) of the medium graph, the fwd+bwd configuration's
+    second half: CUDA events over `steps` calls; returns the dict reported
+    under "backward"."""
+    gen = torch.Generator(device=out.device).manual_seed(7)
+    go = torch.randn((n, desc.dim_out), device=out.device, generator=gen)
+    counts = inp["row_ptr"][1:] - inp["row_ptr"][:-1]
+    dst = torch.repeat_interleave(torch.arange(n, device=out.device, dtype=torch.int32), counts.long())
+    src_perm, src_row_ptr, _ = tpc.tp_csr_build(inp["src"], n)
+    dx = torch.empty((n, desc.dim_x), device=out.device)
+    dw = torch.empty((E, desc.weight_numel), device=out.device)
+    dsh = torch.empty((E, desc.dim_sh), device=out.device)
+
+    def bwd():
+        tpc.tp_conv_backward(desc, go, inp["x"], inp["sh"], inp["w"], inp["src"], dst, inp["row_ptr"], src_perm,
+                             src_row_ptr, dx=dx, dw=dw, dsh=dsh, stream=stream)
+
+    for _ in range(3):
+        bwd()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        bwd()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bwd_us = e0.elapsed_time(e1) / steps * 1e3
+    if tpc.tp_device_status(reset=True) != 0:
+        raise RuntimeError("device status set during the backward timing")
+    nbytes = backward_bytes(desc, n, E)
+    return {"bwd_us": bwd_us, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (bwd_us * 1e-6) / 1e9,
+            "steps": steps, "kernels": "seg_conv_kernel (dw, dsh by destination; dx by source)"}
 
 
 def cpu_baseline(wl, host, n, target_s: float):
@@ -365,6 +408,10 @@ def bench_ours(args):
         "gpu_launches": steps * launches_per_step,
         "clocks": clocks,
     }
+    if args.workload == "medium" and not args.no_backward and wl.dtype == "f32":
+        bk = time_backward(desc, inp, n, E, out, ws, stream, tpc, torch)
+        bk["frac"] = bk["achieved_gbs"] / peak
+        line["backward"] = bk
     if rank == 0 and not args.no_cpu_baseline:
         v, cores, sample = cpu_baseline(wl, host, n, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "edges/s", "cores": cores, "kind": "oracle", "sample": sample}

@@ -1,0 +1,63 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times: the medium, large (bf16) and very large workloads are built exactly as
+the benchmark builds them, the forward runs with its default workspace (the
+warp-ring kernel), and sampled destination rows - random ones, the first, the
+last and the one with the most edges - are recomputed one by one by the fp64 C
+oracle from the host copies of the same inputs (the bf16 ones after the same
+round-to-nearest-even), with harmonics from the oracle's own code."""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import BF16_TOL, FP32_TOL, deg_tol, err
+from oracle import cref, so3, tp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_rows(rng, row_ptr, n, k=48):
+    deg = np.diff(row_ptr)
+    rows = set(rng.choice(n, size=min(k, n), replace=False).tolist())
+    rows.update([0, n - 1, int(np.argmax(deg))])
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["medium", "large", "xlarge"])
+def test_fullsize_sampled_rows(tpc, name):
+    import bench
+    dev = torch.device("cuda:0")
+    wl, desc, inp, n, E, host = bench.build_inputs(name, 0, tpc, torch, dev)
+    x, w, src, dst, vec = host
+    out = tpc.tp_conv_forward(desc, inp["x"], inp["sh"], inp["w"], inp["src"], inp["row_ptr"], n)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+
+    plan = tp.Plan(wl.irreps_in, wl.irreps_sh, wl.irreps_out)
+    order = np.argsort(dst, kind="stable")
+    row_ptr = np.zeros(n + 1, dtype=np.int64)
+    np.cumsum(np.bincount(dst, minlength=n), out=row_ptr[1:])
+    rows = _sample_rows(np.random.default_rng(123), row_ptr, n)
+    sel = np.concatenate([order[row_ptr[r]:row_ptr[r + 1]] for r in rows])
+    lrp = np.zeros(len(rows) + 1, dtype=np.int64)
+    np.cumsum(row_ptr[rows + 1] - row_ptr[rows], out=lrp[1:])
+    if wl.dtype == "bf16":   # the values the GPU multiplies
+        xs = torch.as_tensor(x).to(torch.bfloat16).double().numpy()
+        ws = torch.as_tensor(w[sel]).to(torch.bfloat16).double().numpy()
+    else:
+        xs, ws = x.astype(np.float64), w[sel].astype(np.float64)
+    sh = so3.sh_concat([t.l for t in plan.irr_sh], vec[sel].astype(np.float64))
+    ref = cref.conv_forward(plan, xs, sh, ws, src[sel], lrp, len(rows))
+    got = out[torch.as_tensor(rows, device=dev)].double().cpu().numpy()
+    deg = row_ptr[rows + 1] - row_ptr[rows]
+    assert err(got, ref) <= (BF16_TOL if wl.dtype == "bf16" else FP32_TOL)
+    for g, r, d in zip(got, ref, deg):   # every row against its own magnitude, fp32 math on both
+        if d:
+            assert err(g, r) <= deg_tol(int(d))
+        else:
+            assert not np.any(g)
