@@ -183,14 +183,17 @@ TPCONV_API int64_t tp_csr_build_noalloc_max_edges(void);
  *        destinations without edges);
  *   workspace: device memory of tp_conv_forward_workspace_size() bytes
  *        (256-byte aligned), or NULL. It holds the partial rows of destinations
- *        that straddle the kernel's exact, edge-balanced split of the edge list;
- *        with NULL (or too small) the library uses its generic kernel, which
- *        needs none but splits work per destination.
+ *        that straddle the kernel's exact, edge-balanced split of the edge list
+ *        into pieces (0 bytes are reported when the descriptor has no split
+ *        kernel). A smaller workspace makes the split use fewer pieces; with
+ *        NULL, or when sh is not 16-byte aligned, the library uses its generic
+ *        kernel, which needs none but splits work per destination.
  * x, w and out must be 16-byte aligned; dim_x*sizeof(x) and
  * weight_numel*sizeof(w) must be multiples of 16 (they are whenever mul % 8
- * == 0). Out-of-range src entries are skipped and set TP_DEV_ERR_INDEX.
- * Summation order is fixed: results are bitwise reproducible run to run on
- * one device (the split depends on the device's SM count). */
+ * == 0). An out-of-range src entry sets TP_DEV_ERR_INDEX and its edge adds
+ * nothing. Summation order is fixed: results are bitwise reproducible run to
+ * run on one device (the split depends on the device's SM count and on the
+ * workspace size). */
 TPCONV_API tp_status tp_conv_forward_workspace_size(const tp_desc *desc, tp_dtype dtype, int32_t N_dst, int64_t E,
                                                     size_t *bytes);
 TPCONV_API tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const void *x, const float *sh,
