@@ -15,8 +15,6 @@ struct ChunkMeta {
     int32_t e0;     // first edge slot of the chunk
     int32_t n;      // edges in the chunk (0 for an empty segment)
     uint32_t bits;  // bit0 valid, bit1 first of segment, bit2 last of segment; bits 8.. edge-valid mask
-    int32_t seg_lead;  // program-kernel producer: floats before the chunk's first harmonic row in the stage
-    int32_t pad_[3];
 };
 constexpr uint32_t kValid = 1u, kFirst = 2u, kLast = 4u;
 

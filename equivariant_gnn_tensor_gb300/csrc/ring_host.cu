@@ -38,9 +38,10 @@ static int env_int(const char *name, int dflt) {
     return v && *v ? std::atoi(v) : dflt;
 }
 
-static size_t carry_bytes(int streams, int dim_out) {
-    const size_t a = (size_t)2 * streams * dim_out * sizeof(float);
-    return (a + 255) / 256 * 256 + (size_t)2 * streams * sizeof(int32_t);
+// head and tail partial rows of every piece, then their destination ids
+static size_t carry_bytes(int pieces, int dim_out) {
+    const size_t a = (size_t)2 * pieces * dim_out * sizeof(float);
+    return (a + 255) / 256 * 256 + (size_t)2 * pieces * sizeof(int32_t);
 }
 
 struct RingLaunch {
