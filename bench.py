@@ -2,15 +2,21 @@
 
 One step = one pass of the whole hot path (segment lookup, gather, per-edge
 weight/harmonic stream, fused all-path contraction, segmented sum and store)
-over the medium workload: N=4096 nodes of a radius graph (r=5, mean degree
-32, E=131064 destination-sorted edges), 128x0e+128x1o+128x2e features,
-harmonics 0e+1o+2e+3o, fp32, per-edge weights N(0,1)/sqrt(13).
+over one workload. The headline line is the largest single-GPU workload, the
+very large one: N=262144 nodes of a radius graph (r=5, mean degree 32,
+E=8390944 destination-sorted edges), 32x0e+32x1o features, harmonics 0e+1o+2e,
+outputs 32x0e+32x1o+32x2e, fp32, per-edge weights N(0,1) (8.29 GB of
+compulsory bytes per step). The same JSON line embeds, each timed on its own,
+the medium (fp32, 13 paths, mul 128) and large (bf16 x and w, 23 paths,
+mul 64) workloads, the tiny workload's per-call latency, and the backward
+(dx, dw, dsh) of the medium graph.
 
 Prints ONE JSON line (rank 0). Inputs are synthetic (seeded), resident in HBM
-before the timed region; the per-step input (0.92 GB, dominated by the weight
-stream) is larger than the 129 MB L2, so no flush is needed.
+before each timed region; every per-step input is larger than the 129 MB L2,
+so no flush is needed.
 
-  python bench.py [--steps K] [--warmup W] [--workload medium|large|xlarge|tiny]
+  python bench.py [--steps K] [--warmup W] [--workload xlarge|large|medium|tiny]
+                  [--configs medium,large,tiny | --configs ""]
   python bench.py --impl reference      # the fp64 CPU oracle timed on the host cores
   torchrun --nproc-per-node N bench.py --gpus N   # N independent replicas (weak scaling)
 """
@@ -41,12 +47,14 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="medium", choices=["tiny", "medium", "large", "xlarge"])
+    ap.add_argument("--workload", default="xlarge", choices=["tiny", "medium", "large", "xlarge"])
+    ap.add_argument("--configs", default="medium,large,tiny",
+                    help="other workloads timed into the same line (comma list; empty for none)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--no-backward", action="store_true", help="skip the backward timing (medium only)")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward timing (medium graph)")
     return ap.parse_args()
 
 
@@ -153,13 +161,15 @@ class ClockSampler:
 
 
 def build_inputs(wname: str, seed: int, tpc, torch, device):
-    """Synthetic inputs of a workload, resident on `device`."""
+    """Synthetic inputs of a workload, resident on `device`. Returns (wl, desc,
+    inputs, n, E, host) with host = (x, w, src, dst, vec, grad_out) as drawn
+    (grad_out None unless the workload has a backward)."""
     from workloads import WORKLOADS, make_features, make_graph
     wl = WORKLOADS[wname]
     desc = tpc.tp_desc_create(wl.irreps_in, wl.irreps_sh, wl.irreps_out)
     rng, src, dst, vec, n = make_graph(wl, seed)
     E = len(src)
-    x, w, _ = make_features(rng, wl, n, E, desc.dim_x, desc.weight_numel, desc.n_paths, desc.dim_out,
+    x, w, g = make_features(rng, wl, n, E, desc.dim_x, desc.weight_numel, desc.n_paths, desc.dim_out,
                             dtype=np.float32)
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     d_dst = torch.as_tensor(dst).to(device)
@@ -175,7 +185,23 @@ def build_inputs(wname: str, seed: int, tpc, torch, device):
         row_ptr=row_ptr,
     )
     torch.cuda.synchronize()
-    return wl, desc, inputs, n, E, (x, w, src, dst, vec)
+    return wl, desc, inputs, n, E, (x, w, src, dst, vec, g)
+
+
+def backward_inputs(tpc, torch, inp, n, grad_out):
+    """What tp_conv_backward needs beyond the forward's inputs: grad_out on the
+    device, the sorted destination of every edge and the source CSR of the
+    destination-sorted edge list (tp_csr_build of src)."""
+    dev = inp["x"].device
+    go = torch.as_tensor(grad_out).to(dev).contiguous()
+    counts = inp["row_ptr"][1:] - inp["row_ptr"][:-1]
+    dst = torch.repeat_interleave(torch.arange(n, device=dev, dtype=torch.int32), counts.long())
+    src_perm, src_row_ptr, _ = tpc.tp_csr_build(inp["src"], n)
+    return go, dst, src_perm, src_row_ptr
+
+
+def describe(wl, n, E):
+    return f"{wl.name}: N={n} E={E} {wl.irreps_in} x {wl.irreps_sh} -> {wl.irreps_out} ({wl.dtype})"
 
 
 def algorithmic_bytes(desc, n, E, esz):
@@ -193,18 +219,15 @@ def backward_bytes(desc, n, E):
             + 2 * (n + 1) * 4)
 
 
-def time_backward(desc, inp, n, E, out, ws, stream, tpc, torch, steps: int = 200):
-    """Backward (dx, dw, dsh) of the medium graph, the fwd+bwd configuration's
-    second half: CUDA events over `steps` calls; returns the dict reported
-    under "backward"."""
-    gen = torch.Generator(device=out.device).manual_seed(7)
-    go = torch.randn((n, desc.dim_out), device=out.device, generator=gen)
-    counts = inp["row_ptr"][1:] - inp["row_ptr"][:-1]
-    dst = torch.repeat_interleave(torch.arange(n, device=out.device, dtype=torch.int32), counts.long())
-    src_perm, src_row_ptr, _ = tpc.tp_csr_build(inp["src"], n)
-    dx = torch.empty((n, desc.dim_x), device=out.device)
-    dw = torch.empty((E, desc.weight_numel), device=out.device)
-    dsh = torch.empty((E, desc.dim_sh), device=out.device)
+def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 100):
+    """Backward (dx, dw, dsh) of the medium graph with its own grad_out, the
+    fwd+bwd configuration's second half: CUDA events over `steps` calls;
+    returns the dict reported under "backward"."""
+    go, dst, src_perm, src_row_ptr = backward_inputs(tpc, torch, inp, n, grad_out)
+    dev = inp["x"].device
+    dx = torch.empty((n, desc.dim_x), device=dev)
+    dw = torch.empty((E, desc.weight_numel), device=dev)
+    dsh = torch.empty((E, desc.dim_sh), device=dev)
 
     def bwd():
         tpc.tp_conv_backward(desc, go, inp["x"], inp["sh"], inp["w"], inp["src"], dst, inp["row_ptr"], src_perm,
@@ -227,11 +250,122 @@ def time_backward(desc, inp, n, E, out, ws, stream, tpc, torch, steps: int = 200
             "steps": steps, "kernels": "seg_conv_kernel (dw, dsh by destination; dx by source)"}
 
 
+class Forward:
+    """One workload's inputs on the device and its forward call."""
+
+    def __init__(self, wname, seed, tpc, torch, device, stream):
+        self.tpc, self.torch, self.stream = tpc, torch, stream
+        self.wl, self.desc, self.inp, self.n, self.E, self.host = build_inputs(wname, seed, tpc, torch, device)
+        self.esz = 2 if self.wl.dtype == "bf16" else 4
+        self.out = torch.empty((self.n, self.desc.dim_out), dtype=torch.float32, device=device)
+        fdt = tpc.TP_BF16_IN_F32_OUT if self.wl.dtype == "bf16" else tpc.TP_F32
+        ws_bytes = tpc.tp_conv_forward_workspace_size(self.desc, fdt, self.n, self.E)
+        self.ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device) if ws_bytes else None
+        # the warp-ring kernel + its partial-row merge, or the generic kernel alone
+        self.launches_per_step = 2 if ws_bytes else 1
+        self.abytes = algorithmic_bytes(self.desc, self.n, self.E, self.esz)
+
+    def step(self):
+        i = self.inp
+        self.tpc.tp_conv_forward(self.desc, i["x"], i["sh"], i["w"], i["src"], i["row_ptr"], self.n, out=self.out,
+                                 workspace=self.ws, stream=self.stream)
+
+    def timed(self, steps, warmup, local, world=1, device=None):
+        """CUDA-event time of `steps` back-to-back steps (ms, max over ranks)
+        with nvidia-smi clocks sampled during the timed region."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        if self.tpc.tp_device_status(reset=True) != 0:
+            raise RuntimeError("device status set during warm-up")
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(self.stream)
+        for _ in range(steps):
+            self.step()
+        ev1.record(self.stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clocks = sampler.stop()
+        ms_local = ev0.elapsed_time(ev1)
+        if self.tpc.tp_device_status(reset=True) != 0:
+            raise RuntimeError("device status set during the timed region")
+        return max_over_ranks(ms_local, world, device), ms_local, clocks
+
+    def roofline(self, kernel_ms, peak, peak_src, key):
+        achieved = self.abytes / (kernel_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(key), "algorithmic_bytes": self.abytes, "kernel_us": kernel_ms * 1e3,
+                "peak_source": peak_src}
+
+    def describe(self):
+        return describe(self.wl, self.n, self.E)
+
+    def e2e(self, steps):
+        """The same forward through the public call with the inputs in pinned
+        host memory: host->device copies of every input, the call, and the
+        device->host copy of out, all inside the timed region."""
+        torch = self.torch
+        pin = {k: v.cpu().pin_memory() for k, v in self.inp.items()}
+        out_h = torch.empty_like(self.out, device="cpu").pin_memory()
+        dev_bufs = {k: torch.empty_like(v) for k, v in self.inp.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = self.out.numel() * self.out.element_size()
+
+        def e2e_step():
+            for k in pin:
+                dev_bufs[k].copy_(pin[k], non_blocking=True)
+            self.tpc.tp_conv_forward(self.desc, dev_bufs["x"], dev_bufs["sh"], dev_bufs["w"], dev_bufs["src"],
+                                     dev_bufs["row_ptr"], self.n, out=self.out, workspace=self.ws, stream=self.stream)
+            out_h.copy_(self.out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(steps):
+            e2e_step()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        del pin, dev_bufs
+        return e0.elapsed_time(e1), h2d, d2h
+
+
+def tiny_latency(tpc, torch, device, stream, calls: int = 20000):
+    """The tiny workload (512 edges) is launch-bound: per-call device time
+    (CUDA events over back-to-back calls) and per-call host time of the public
+    Python call (wall clock, including the ctypes marshalling)."""
+    f = Forward("tiny", 0, tpc, torch, device, stream)
+    for _ in range(100):
+        f.step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        f.step()
+    t1 = time.perf_counter()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    gpu_us = e0.elapsed_time(e1) / calls * 1e3
+    return {"workload": f.describe(), "calls": calls, "us_per_call_device": gpu_us,
+            "us_per_call_host": (t1 - t0) / calls * 1e6, "edges_per_s": f.E / (gpu_us * 1e-6),
+            "launches_per_call": f.launches_per_step,
+            "note": "launch-bound (0.53 MB of compulsory bytes): reported as latency, not against the roofline"}
+
+
 def cpu_baseline(wl, host, n, target_s: float):
     """The oracle (plain C, fp64, OpenMP) on a bounded sample of destination
     rows of the same workload; returns (edges/s, cores, description)."""
     from oracle import cref, so3, tp
-    x, w, src, dst, vec = host
+    x, w, src, dst, vec = host[:5]
     plan = tp.Plan(wl.irreps_in, wl.irreps_sh, wl.irreps_out)
     cores = len(os.sched_getaffinity(0))
     order = np.argsort(dst, kind="stable")
@@ -250,16 +384,14 @@ def cpu_baseline(wl, host, n, target_s: float):
             cref.conv_forward(plan, xs, sh, ws, src[sel], lrp, len(rows), threads=cores)
         return time.perf_counter() - t0, len(sel)
 
-    rows = np.arange(min(n, 32))
-    dt, ne = run(rows)                       # warm-up + calibration
-    scale = max(1.0, target_s / max(dt, 1e-3))
-    k = int(min(n, max(32, len(rows) * scale)))
+    # the first destination rows holding at most 2^21 edges (bounded host
+    # memory), repeated for about target_s seconds
+    k = int(np.searchsorted(row_ptr, 1 << 21, side="right")) - 1
+    k = max(1, min(n, k))
     rows = np.arange(k)
-    dt, ne = run(rows)
-    reps = 1
-    if k == n and dt < 0.5 * target_s:      # the whole workload is quick: repeat it
-        reps = int(min(200, max(1, target_s / max(dt, 1e-3))))
-        dt, ne = run(rows, reps)
+    dt, ne = run(rows)                       # warm-up + calibration
+    reps = int(min(200, max(1, math.ceil(target_s / max(dt, 1e-3)))))
+    dt, ne = run(rows, reps)
     what = f"first {k} destination rows" if k < n else f"all {n} destination rows"
     return ne * reps / dt, cores, f"{what} ({ne} edges) x {reps} of the workload, fp64 oracle, {dt:.1f} s"
 
@@ -281,7 +413,8 @@ def bench_reference(args):
     order = np.argsort(dst, kind="stable")
     row_ptr = np.zeros(n + 1, dtype=np.int64)
     np.cumsum(np.bincount(dst, minlength=n), out=row_ptr[1:])
-    n_rows = min(n, 64)
+    # per step: the first destination rows holding at most 2^16 edges
+    n_rows = max(1, min(n, int(np.searchsorted(row_ptr, 1 << 16, side="right")) - 1))
     sel = order[:row_ptr[n_rows]]
     sh = so3.sh_concat([t.l for t in plan.irr_sh], vec[sel])
     xs, ws = x.astype(np.float64), w[sel].astype(np.float64)
@@ -299,13 +432,15 @@ def bench_reference(args):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "edges/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: N={n} E={E} {wl.irreps_in} x {wl.irreps_sh}",
-                   "sample": f"first {n_rows} destination rows ({ne} edges) per step"},
+        "config": {"workload": describe(wl, n, E), "sample": f"first {n_rows} destination rows ({ne} edges) per step"},
         "cpu_baseline": {"value": val, "unit": "edges/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {n_rows} destination rows ({ne} edges) of {args.workload}, fp64 C oracle"},
         "e2e": {"value": val, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+DEFAULT_STEPS = {"tiny": 20000, "medium": 2000, "large": 300, "xlarge": 500}
 
 
 def bench_ours(args):
@@ -319,101 +454,64 @@ def bench_ours(args):
     torch.cuda.set_device(device)
     import equivariant_gnn_tensor_gb300 as tpc
 
-    wl, desc, inp, n, E, host = build_inputs(args.workload, args.seed + rank, tpc, torch, device)
-    esz = 2 if wl.dtype == "bf16" else 4
-    steps = args.steps if args.steps is not None else {"tiny": 20000, "medium": 6000, "large": 600,
-                                                       "xlarge": 600}[args.workload]
-    warmup = max(3, args.warmup)
-    out = torch.empty((n, desc.dim_out), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    fdt = tpc.TP_BF16_IN_F32_OUT if wl.dtype == "bf16" else tpc.TP_F32
-    ws_bytes = tpc.tp_conv_forward_workspace_size(desc, fdt, n, E)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device) if ws_bytes else None
-    launches_per_step = 2 if ws_bytes else 1   # split kernel + partial merge, or the generic kernel
-
-    def step():
-        tpc.tp_conv_forward(desc, inp["x"], inp["sh"], inp["w"], inp["src"], inp["row_ptr"], n, out=out,
-                            workspace=ws, stream=stream)
-
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    if tpc.tp_device_status(reset=True) != 0:
-        raise RuntimeError("device status set during warm-up")
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop()
-    ms_local = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms_local, world, device)
-    kernel_ms = ms_local / steps     # per step: the forward kernel (+ the tiny partial merge)
-    value = E * steps * world / (ms / 1e3)
-
-    # end to end through the public call with host buffers (pinned), copies inside the timed region
-    pin = {k: v.cpu().pin_memory() for k, v in inp.items()}
-    out_h = torch.empty_like(out, device="cpu").pin_memory()
-    dev_bufs = {k: torch.empty_like(v) for k, v in inp.items()}
-    h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = out.numel() * out.element_size()
-
-    def e2e_step():
-        for k in pin:
-            dev_bufs[k].copy_(pin[k], non_blocking=True)
-        tpc.tp_conv_forward(desc, dev_bufs["x"], dev_bufs["sh"], dev_bufs["w"], dev_bufs["src"],
-                            dev_bufs["row_ptr"], n, out=out, workspace=ws, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-    e2e_val = E * args.e2e_steps * world / (e2e_ms / 1e3)
-    status = tpc.tp_device_status(reset=True)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
-
     peak, peak_src = measured_peaks()
-    abytes = algorithmic_bytes(desc, n, E, esz)
-    achieved = abytes / (kernel_ms * 1e-3) / 1e9
-    key = f"fwd:{args.workload}"
+    warmup = max(3, args.warmup)
+
+    # ---- headline workload -------------------------------------------------------
+    f = Forward(args.workload, args.seed + rank, tpc, torch, device, stream)
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    ms, ms_local, clocks = f.timed(steps, warmup, local, world, device)
+    kernel_ms = ms_local / steps
+    value = f.E * steps * world / (ms / 1e3)
+    e2e_ms, h2d, d2h = f.e2e(args.e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e_val = f.E * args.e2e_steps * world / (e2e_ms / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world, "steps": steps, "warmup": warmup,
         "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: N={n} E={E} {wl.irreps_in} x {wl.irreps_sh} -> {wl.irreps_out}",
-                   "paths": desc.n_paths, "weight_numel": desc.weight_numel,
+        "dtype": "bf16" if f.wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": f.describe(), "paths": f.desc.n_paths, "weight_numel": f.desc.weight_numel,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": f"per-step input {abytes / 1e9:.2f} GB > 129 MB L2 (no flush needed)"},
-        "hbm_gbs": achieved,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": profiled_traffic(key), "algorithmic_bytes": abytes,
-                     "kernel_us": kernel_ms * 1e3, "peak_source": peak_src},
+                   "l2": f"per-step input {f.abytes / 1e9:.2f} GB > 129 MB L2 (no flush needed)"},
+        "hbm_gbs": f.abytes / (kernel_ms * 1e-3) / 1e9,
+        "roofline": f.roofline(kernel_ms, peak, peak_src, f"fwd:{args.workload}"),
         "e2e": {"value": e2e_val, "unit": "edges/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": steps * launches_per_step,
+        "gpu_launches": steps * f.launches_per_step,
         "clocks": clocks,
     }
-    if args.workload == "medium" and not args.no_backward and wl.dtype == "f32":
-        bk = time_backward(desc, inp, n, E, out, ws, stream, tpc, torch)
-        bk["frac"] = bk["achieved_gbs"] / peak
-        line["backward"] = bk
+    host, wl_head, head_n = f.host, f.wl, f.n
+    del f
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, each timed on its own (single GPU runs only) --------
+    if world == 1:
+        cfgs = {}
+        for name in [c for c in args.configs.split(",") if c and c != args.workload]:
+            if name == "tiny":
+                cfgs["tiny"] = tiny_latency(tpc, torch, device, stream)
+                continue
+            g = Forward(name, args.seed, tpc, torch, device, stream)
+            k = DEFAULT_STEPS[name]
+            _, ms_c, clk = g.timed(k, warmup, local)
+            cfgs[name] = {"workload": g.describe(), "value": g.E * k / (ms_c / 1e3), "unit": "edges/s",
+                          "steps": k, "kernel_us": ms_c / k * 1e3,
+                          "roofline": g.roofline(ms_c / k, peak, peak_src, f"fwd:{name}"), "clocks": clk,
+                          "gpu_launches": k * g.launches_per_step}
+            del g
+            torch.cuda.empty_cache()
+        line["configs"] = cfgs
+        if not args.no_backward:
+            # the fwd+bwd workload: the medium graph and features with its own grad_out
+            b = Forward("fwdbwd", args.seed, tpc, torch, device, stream)
+            bk = time_backward(tpc, torch, b.desc, b.inp, b.n, b.E, b.host[5], stream)
+            bk["frac"] = bk["achieved_gbs"] / peak
+            bk["workload"] = b.describe()
+            line["backward"] = bk
+            del b
+            torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
-        v, cores, sample = cpu_baseline(wl, host, n, args.cpu_seconds)
+        v, cores, sample = cpu_baseline(wl_head, host, head_n, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "edges/s", "cores": cores, "kind": "oracle", "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -32,7 +32,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 TP_OK = 0
-STATUS_NAMES = {0: "TP_OK", 1: "TP_ERR_PARSE", 2: "TP_ERR_UNSUPPORTED", 3: "TP_ERR_UNSORTED", 4: "TP_ERR_INDEX",
+STATUS_NAMES = {0: "TP_OK", 1: "TP_ERR_PARSE", 2: "TP_ERR_UNSUPPORTED", 4: "TP_ERR_INDEX",
                 5: "TP_ERR_ALIGN", 6: "TP_ERR_CUDA", 7: "TP_ERR_ARG", 8: "TP_ERR_TIMEOUT", 9: "TP_ERR_CAPACITY"}
 TP_F32, TP_BF16_IN_F32_OUT = 0, 1
 TP_IR_MUL, TP_MUL_IR = 0, 1
@@ -40,7 +40,8 @@ TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
 EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
            "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
            "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
-           "tp_conv_backward", "tp_device_status", "tp_status_string", "tp_abi_version"]
+           "tp_conv_backward", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
+           "tp_abi_version"]
 
 
 class TPError(RuntimeError):
@@ -54,6 +55,12 @@ class _Info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_paths", "mul", "dim_x", "dim_sh", "dim_out", "weight_numel", "n_in", "n_sh", "n_out",
         "lmax_in", "lmax_sh", "lmax_out", "cg_nnz")]
+
+
+class _Tuning(ctypes.Structure):
+    _fields_ = [("ring_stage_bytes", ctypes.c_int32), ("ring_stages", ctypes.c_int32), ("ring_warps", ctypes.c_int32),
+                ("ring_rounds", ctypes.c_int32), ("ring_pack", ctypes.c_int32), ("disable_split", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64)]
 
 
 class _Path(ctypes.Structure):
@@ -74,6 +81,8 @@ _sigs = {
     "tp_conv_forward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _sz, _vp],
     "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
+    "tp_set_tuning": [ctypes.POINTER(_Tuning)],
+    "tp_get_tuning": [ctypes.POINTER(_Tuning)],
 }
 for _n, _a in _sigs.items():
     getattr(_lib, _n).argtypes = _a
@@ -230,8 +239,9 @@ def tp_csr_build_noalloc_max_edges() -> int:
 
 def tp_csr_build_noalloc(keys, N: int, perm, row_ptr, keys_sorted=None, stream=None):
     """tp_csr_build without any device allocation, for callers that cannot
-    allocate (a stream being captured into a CUDA graph, a plugin's enqueue):
-    the caller passes every output buffer and the library uses its own fixed
+    allocate device memory themselves (a plugin's enqueue callback handed only
+    its tensors, a program whose memory belongs to another allocator): the
+    caller passes every output buffer and the library uses its own fixed
     scratch array (E <= tp_csr_build_noalloc_max_edges()). Calls that overlap
     on the GPU share that array and race."""
     torch = _torch()
@@ -308,6 +318,29 @@ def tp_conv_backward(desc: Descriptor, grad_out, x, sh, w, src, dst, row_ptr, sr
                                  _stream(stream)),
            "tp_conv_backward")
     return dx, dw, dsh
+
+
+TUNING_FIELDS = [f for f, _ in _Tuning._fields_]
+
+
+def tp_set_tuning(**fields):
+    """Process-wide launch tuning / test hooks (see tp_tuning in the header);
+    fields not given keep the library default. With no arguments every
+    default is restored."""
+    bad = set(fields) - set(TUNING_FIELDS)
+    if bad:
+        raise TypeError(f"unknown tuning fields {sorted(bad)}")
+    if not fields:
+        _check(_lib.tp_set_tuning(None), "tp_set_tuning")
+        return
+    t = _Tuning(**{k: int(v) for k, v in fields.items()})
+    _check(_lib.tp_set_tuning(ctypes.byref(t)), "tp_set_tuning")
+
+
+def tp_get_tuning() -> dict:
+    t = _Tuning()
+    _check(_lib.tp_get_tuning(ctypes.byref(t)), "tp_get_tuning")
+    return {f: int(getattr(t, f)) for f in TUNING_FIELDS}
 
 
 def tp_device_status(reset: bool = True, stream=None) -> int:

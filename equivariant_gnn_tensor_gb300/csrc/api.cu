@@ -10,6 +10,7 @@
 
 #include "../../include/tpconv.h"
 #include "launch.h"
+#include "tuning.h"
 
 namespace tpc {
 size_t csr_workspace_bytes(int64_t E, int32_t N);
@@ -18,11 +19,21 @@ cudaError_t csr_build_launch(const int32_t *keys, int64_t E, int32_t N, int32_t 
 cudaError_t sh_launch(const float *vec, int64_t E, int normalize, const Tables &T, float *sh, cudaStream_t stream);
 int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
-size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin);
+size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
 cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
                          const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
-                         float *out, void *ws, size_t ws_bytes, int sms, int smem_optin, int *status,
+                         float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
                          cudaStream_t stream);
+
+// ---- process-wide tuning (tp_set_tuning) ----
+static std::mutex g_tune_mu;
+static tp_tuning g_tune = {};
+static uint32_t g_tune_gen = 1;
+
+TuningState tuning_snapshot() {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    return TuningState{g_tune, g_tune_gen};
+}
 }  // namespace tpc
 
 namespace {
@@ -35,6 +46,7 @@ static_assert(sizeof(SegParams) <= 32000, "kernel parameter block too large");
 __device__ int g_tp_status;
 
 struct DevInfo {
+    int dev = 0;
     int sms = 0;
     int smem_optin = 0;
     int *status = nullptr;
@@ -54,6 +66,7 @@ tp_status dev_info(DevInfo &out) {
         return TP_OK;
     }
     DevInfo d;
+    d.dev = dev;
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TP_ERR_CUDA;
     if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return TP_ERR_CUDA;
@@ -114,6 +127,8 @@ tp_status plan_launch(const void *fn, const DevInfo &dev, int head_bytes, int w_
 }
 
 tp_status launch_seg(const void *fn, SegParams &prm, int grid, int warps, int smem, cudaStream_t stream) {
+    const TuningState ts = tuning_snapshot();
+    prm.wait_ns = ts.t.wait_limit_ns > 0 ? (uint64_t)ts.t.wait_limit_ns : kWaitNs;
     void *args[] = {&prm};
     if (cudaLaunchKernel(fn, dim3(grid), dim3(warps * 32), args, (size_t)smem, stream) != cudaSuccess)
         return TP_ERR_CUDA;
@@ -179,7 +194,7 @@ extern "C" tp_status tp_conv_forward_workspace_size(const tp_desc *desc, tp_dtyp
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
-    *bytes = split_workspace_bytes(desc, dtype, E, dev.sms, dev.smem_optin);
+    *bytes = split_workspace_bytes(desc, dtype, E, dev.dev, dev.sms, dev.smem_optin);
     return TP_OK;
 }
 
@@ -204,7 +219,7 @@ extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
         tp_status st = dev_info(dev);
         if (st != TP_OK) return st;
         const cudaError_t e = split_forward(desc, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, workspace,
-                                           workspace_bytes, dev.sms, dev.smem_optin, dev.status,
+                                           workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
                                            static_cast<cudaStream_t>(stream));
         if (e == cudaSuccess) return TP_OK;
         if (e != cudaErrorNotSupported) return TP_ERR_CUDA;
@@ -310,6 +325,29 @@ extern "C" tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out
     return TP_OK;
 }
 
+extern "C" tp_status tp_set_tuning(const tp_tuning *t) {
+    tp_tuning v = {};
+    if (t) {
+        v = *t;
+        const bool ok = v.ring_stage_bytes >= 0 && (v.ring_stages == 0 || (v.ring_stages >= 2 && v.ring_stages <= 8)) &&
+                        (v.ring_warps == 0 || (v.ring_warps >= 1 && v.ring_warps <= kRingMaxWarps)) &&
+                        (v.ring_rounds == 0 || (v.ring_rounds >= 1 && v.ring_rounds <= kRingMaxPiecesPerWarp)) &&
+                        v.ring_pack >= 0 && v.ring_pack <= 2 && (v.disable_split == 0 || v.disable_split == 1) &&
+                        v.wait_limit_ns >= 0;
+        if (!ok) return TP_ERR_ARG;
+    }
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    g_tune = v;
+    ++g_tune_gen;
+    return TP_OK;
+}
+
+extern "C" tp_status tp_get_tuning(tp_tuning *t) {
+    if (!t) return TP_ERR_ARG;
+    *t = tuning_snapshot().t;
+    return TP_OK;
+}
+
 extern "C" tp_status tp_device_status(int32_t *flags, int32_t reset, void *stream) {
     if (!flags) return TP_ERR_ARG;
     DevInfo dev;
@@ -329,7 +367,6 @@ extern "C" const char *tp_status_string(tp_status s) {
         case TP_OK: return "ok";
         case TP_ERR_PARSE: return "irreps string cannot be parsed";
         case TP_ERR_UNSUPPORTED: return "configuration not supported by the kernels";
-        case TP_ERR_UNSORTED: return "row pointers not sorted";
         case TP_ERR_INDEX: return "index out of range";
         case TP_ERR_ALIGN: return "pointer or row size not 16-byte aligned";
         case TP_ERR_CUDA: return "CUDA runtime error";

@@ -11,7 +11,9 @@
 namespace tpc {
 
 // An mbarrier wait gives up after about this long, so a lost copy turns into a
-// status bit instead of a hung GPU.
+// status bit instead of a hung GPU. Kernels take their main-loop limit as a
+// parameter (this value unless a test shortens it); the waits that let copies
+// in flight land before a failed warp exits always use this one.
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -77,15 +79,16 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
     return ok != 0;
 }
 
-// Bounded wait: true when the phase completed, false after about kWaitNs.
-// The clock is read only once the phase was found incomplete, and then only
-// every 64 suspended probes.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Bounded wait: true when the phase completed, false once about `limit_ns`
+// have passed since the first probe found it incomplete. The clock is read
+// only on that slow path, after every suspended probe.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_hint(bar, parity, 2000u)) return true;
-        if ((it & 63u) == 0 && global_ns() - t0 > kWaitNs) return false;
+    const uint32_t hint = limit_ns < 2000u ? (uint32_t)limit_ns : 2000u;
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, hint)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -39,6 +39,7 @@ struct SegParams {
     int32_t n_seg;            // segments
     int32_t n_gather;         // rows of feat
     int64_t n_edges;
+    uint64_t wait_ns;         // main-loop pipeline wait limit
 };
 
 template <int LI, int LO, int CPT, typename FT, int MODE>
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(256, 1) seg_conv_kernel(const __grid_constant_
     bool failed = false;
     for (int s = 0;; s = (s + 1 == L.stages) ? 0 : s + 1) {
         if (!((inflight >> s) & 1u)) break;
-        const bool ok = mbar_wait(&bars[s], (phase >> s) & 1u);
+        const bool ok = mbar_wait(&bars[s], (phase >> s) & 1u, prm.wait_ns);
         if (!__all_sync(0xffffffffu, ok)) {
             failed = true;
             break;
@@ -258,7 +259,14 @@ __global__ void __launch_bounds__(256, 1) seg_conv_kernel(const __grid_constant_
             }
         }
         for (int q = 0; q < m.n; ++q) {
-            if (!((m.bits >> (8 + q)) & 1u)) continue;
+            if (!((m.bits >> (8 + q)) & 1u)) {
+                if constexpr (MODE == kBwdEdge) {  // a skipped edge still gets zero gradient rows
+                    const int64_t e = m.e0 + q;
+                    for (int t = lane; t < T.wnum; t += 32) prm.dw[e * T.wnum + t] = 0.f;
+                    for (int j = lane; j < T.dim_sh; j += 32) prm.dsh[e * T.dim_sh + j] = 0.f;
+                }
+                continue;
+            }
             const FT *fs = reinterpret_cast<const FT *>(sb + L.f_off + q * L.f_bytes);
             const FT *ws = reinterpret_cast<const FT *>(sb + L.w_off + q * L.w_bytes);
             const float *Mq = Ms + q * T.R;
@@ -349,9 +357,10 @@ __global__ void __launch_bounds__(256, 1) seg_conv_kernel(const __grid_constant_
     }
     if (failed) {
         set_status(prm.status, TP_DEV_ERR_TIMEOUT);
-        // let copies still in flight land before the block's shared memory is released
+        // let copies still in flight land (full time limit) before the block's
+        // shared memory is released
         for (int s = 0; s < L.stages; ++s)
-            if ((inflight >> s) & 1u) (void)mbar_wait(&bars[s], (phase >> s) & 1u);
+            if ((inflight >> s) & 1u) (void)mbar_wait(&bars[s], (phase >> s) & 1u, kWaitNs);
     }
 }
 

@@ -12,6 +12,7 @@
 // which is real up to one global phase; the phase is dropped, the tensor is
 // scaled to be orthonormal over (i,j) for each k and its sign fixed so the
 // first entry above 1e-9 in (i,j,k) row-major order is positive.
+#include <atomic>
 #include <cctype>
 #include <cmath>
 #include <complex>
@@ -246,6 +247,7 @@ void plan_program(tp_desc *d) {
 
 void free_desc(tp_desc *d) {
     if (!d) return;
+    tpc::launch_cache_forget(d->uid);
     for (int p = 0; p < d->n_paths; ++p) std::free(d->cg[p]);
     delete d;
 }
@@ -270,6 +272,8 @@ extern "C" tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh
     tp_desc *d = new (std::nothrow) tp_desc();
     if (!d) return TP_ERR_ARG;
     std::memset(d, 0, sizeof(*d));
+    static std::atomic<uint64_t> next_uid{1};
+    d->uid = next_uid.fetch_add(1);
     d->n_in = (int)tin.size();
     d->n_sh = (int)tsh.size();
     d->n_out = (int)tout.size();

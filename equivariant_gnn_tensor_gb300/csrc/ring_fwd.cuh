@@ -39,6 +39,7 @@
 #include "common.cuh"
 #include "conv_common.cuh"
 #include "program.h"
+#include "tuning.h"
 
 namespace tpc {
 
@@ -78,11 +79,11 @@ __device__ __forceinline__ int warp_first_geq(const int32_t *rp, int N, int64_t 
 
 // out[d] = tail partial of the piece where d starts + head partials of the
 // following pieces that continue d, added in piece order. One warp per piece.
+// Destination ids outside [0, n_dst) (a piece a failed warp never reached
+// holds -1) are skipped.
 __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_t *__restrict__ carry_dst, int n_pieces,
-                                   int dim_out, float *__restrict__ out);
+                                   int dim_out, int n_dst, float *__restrict__ out);
 
-constexpr int kRingMaxWarps = 8;
-constexpr int kRingMaxPiecesPerWarp = 16;
 
 struct RingParams {
     int32_t S, eps;                      // stages per warp, edges per chunk (<= 30)
@@ -102,6 +103,7 @@ struct RingParams {
     int *status;
     int32_t n_src, n_dst, n_warps, n_pieces;
     int64_t E;
+    uint64_t wait_ns;    // main-loop pipeline wait limit
 };
 
 // Smallest d in [0, N] with rp[d] >= target (N+1 if none): one lane's binary search.
@@ -553,8 +555,16 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         int e = e_lo;
         while (e < e_hi) {
             const int s = s_done;
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph_done))) {
-                if (lane == 0) set_status(prm.status, TP_DEV_ERR_TIMEOUT);
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph_done, prm.wait_ns))) {
+                if (lane == 0) {
+                    set_status(prm.status, TP_DEV_ERR_TIMEOUT);
+                    // this piece's partial rows and those of the pieces never
+                    // reached are not written: the merge must skip them
+                    for (int j2 = j; j2 < np_w; ++j2) {
+                        prm.carry_dst[2 * (gw + j2 * nW)] = -1;
+                        prm.carry_dst[2 * (gw + j2 * nW) + 1] = -1;
+                    }
+                }
                 failed = true;
                 break;
             }
@@ -664,9 +674,10 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         }
     }
     if (failed) {
-        // let the copies still in flight land before the shared memory is released
+        // let the copies still in flight land (full time limit) before the
+        // shared memory is released
         for (int k = n_done; k < n_issued; ++k) {
-            (void)mbar_wait(&full[s_done], ph_done);
+            (void)mbar_wait(&full[s_done], ph_done, kWaitNs);
             if (++s_done == S) {
                 s_done = 0;
                 ph_done ^= 1u;

@@ -3,10 +3,14 @@
 // piece boundaries, and the partial-merging kernel.
 #include <cuda_runtime.h>
 
-#include <cstdlib>
 #include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <tuple>
 
 #include "ring_fwd.cuh"
+#include "tuning.h"
 
 namespace tpc {
 
@@ -14,12 +18,12 @@ const void *ring_kernel_f32(int shape, int cpt, int pk);
 const void *ring_kernel_bf16(int shape, int cpt, int pk);
 
 __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_t *__restrict__ carry_dst,
-                                   int n_pieces, int dim_out, float *__restrict__ out) {
+                                   int n_pieces, int dim_out, int n_dst, float *__restrict__ out) {
     const int c = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (c >= n_pieces) return;
     const int d = carry_dst[2 * c + 1];
-    if (d < 0) return;
+    if (d < 0 || d >= n_dst) return;
     for (int col = lane * 4; col < dim_out; col += 128) {
         float4 v = *reinterpret_cast<const float4 *>(carry + (int64_t)(2 * c + 1) * dim_out + col);
         for (int c2 = c + 1; c2 < n_pieces && carry_dst[2 * c2] == d; ++c2) {
@@ -33,31 +37,25 @@ __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_
     }
 }
 
-static int env_int(const char *name, int dflt) {
-    const char *v = std::getenv(name);
-    return v && *v ? std::atoi(v) : dflt;
-}
-
 // head and tail partial rows of every piece, then their destination ids
 static size_t carry_bytes(int pieces, int dim_out) {
     const size_t a = (size_t)2 * pieces * dim_out * sizeof(float);
     return (a + 255) / 256 * 256 + (size_t)2 * pieces * sizeof(int32_t);
 }
 
+// The part of a ring launch that does not depend on the edge count: kernel,
+// shared-memory layout, M recipe, warps per block and blocks per SM.
 struct RingLaunch {
     const void *fn = nullptr;
-    RingParams geo{};  // layout fields only
-    int wpb = 0, n_warps = 0, n_pieces = 0, smem = 0;
+    RingParams geo{};  // layout fields and M recipe only
+    int wpb = 0, smem = 0, occ = 0, rounds = 1;
 };
 
 // One warp covers all channels, CPT = mul/32 in {1,2,4} channels per lane,
 // for descriptors in the natural layout the kernel is compiled for.
-// Tunables (environment): TPCONV_RING_STAGE_BYTES (target bytes per chunk),
-// TPCONV_RING_STAGES, TPCONV_RING_WARPS (warps per block), TPCONV_RING_ROUNDS
-// (pieces per warp), TPCONV_RING_PACK (packed FMAs over channel or edge pairs).
-static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin, RingLaunch &rl) {
+static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp_tuning &tu, RingLaunch &rl) {
     const ProgramPlan &TP = d->prog;
-    if (!TP.valid || E >= (int64_t)1 << 31) return false;  // 32-bit edge indices inside the kernel
+    if (!TP.valid) return false;
     const Tables &T = d->tab;
     const int mul = T.mul;
     if (mul % 32 != 0) return false;
@@ -66,7 +64,7 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int 
     // packed FMAs: channel pairs for two channels per lane, edge pairs for one
     // (the two smaller programs; the larger ones run out of registers); four
     // channels per lane keep plain FMAs (shorter dependent latency)
-    const int pk = env_int("TPCONV_RING_PACK", cpt == 4 ? 0 : (cpt == 2 || TP.shape <= 1)) != 0;
+    const int pk = tu.ring_pack ? (tu.ring_pack == 1) : (cpt == 4 ? 0 : (cpt == 2 || TP.shape <= 1));
     // natural layout: block l at l*l*mul, paths in program order
     const ProgShape shp = kProgShapes[TP.shape];
     const Program prog = make_natural_program(shp.li, shp.lsh, shp.lo);
@@ -83,94 +81,91 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int 
     if (!rl.fn) return false;
     const int esz = dtype == TP_F32 ? 4 : 2;
     RingParams &g = rl.geo;
+    std::memset(&g, 0, sizeof(g));
     const int w_bytes = T.wnum * esz, f_bytes = T.dim_x * esz;
     const int shn = T.dim_sh;
     const int per_edge = w_bytes + f_bytes + shn * 4;
     // about 4.5 KB per chunk and two stages per warp: one chunk lands while the
     // warp works on the other, and enough warps fit on an SM to keep HBM busy
-    const int target = env_int("TPCONV_RING_STAGE_BYTES", 4500);
+    const int target = tu.ring_stage_bytes ? tu.ring_stage_bytes : 4500;
     int eps = (target + per_edge - 1) / per_edge;
     eps = eps < 1 ? 1 : (eps > 30 ? 30 : eps);  // lanes 2..31 issue the gathered rows
-    int S = env_int("TPCONV_RING_STAGES", 2);
-    S = S < 2 ? 2 : (S > 8 ? 8 : S);
-    g.S = S;
+    g.S = tu.ring_stages ? tu.ring_stages : 2;
     g.eps = eps;
     g.f_off = eps * w_bytes;
     g.sh_off = g.f_off + eps * f_bytes;
     g.stage_bytes = round_up(g.sh_off + eps * shn * 4 + 32, 128);  // +32: 16-byte aligned harmonic span
-    g.m_off = S * g.stage_bytes;
+    g.m_off = g.S * g.stage_bytes;
     g.bar_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
-    g.warp_bytes = round_up(g.bar_off + S * 8, 128);
+    g.warp_bytes = round_up(g.bar_off + g.S * 8, 128);
     g.tab_bytes = round_up(16 * TP.R, 128);
-    int wpb = env_int("TPCONV_RING_WARPS", 8);
-    wpb = wpb < 1 ? 1 : (wpb > kRingMaxWarps ? kRingMaxWarps : wpb);
+    std::memcpy(g.ej, TP.ej, sizeof(uint32_t) * TP.R);
+    std::memcpy(g.ec, TP.ec, sizeof(float) * 2 * TP.R);
+    int wpb = tu.ring_warps ? tu.ring_warps : 8;
     while (wpb > 1 && g.tab_bytes + wpb * g.warp_bytes > smem_optin) --wpb;
     rl.smem = g.tab_bytes + wpb * g.warp_bytes;
     if (rl.smem > smem_optin) return false;
     rl.wpb = wpb;
     if (cudaFuncSetAttribute(rl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess) return false;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rl.fn, 32 * wpb, rl.smem) != cudaSuccess || occ < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rl.occ, rl.fn, 32 * wpb, rl.smem) != cudaSuccess || rl.occ < 1)
         return false;
-    long long nw = (long long)sms * occ * wpb;
-    const long long by_edges = (E + 63) / 64;  // at least ~64 edges per warp
-    if (nw > by_edges) nw = by_edges;
-    if (nw < 1) nw = 1;
-    int rounds = env_int("TPCONV_RING_ROUNDS", 1);
-    rounds = rounds < 1 ? 1 : (rounds > kRingMaxPiecesPerWarp ? kRingMaxPiecesPerWarp : rounds);
-    rl.n_warps = (int)nw;
-    rl.n_pieces = (int)nw * rounds;
+    rl.rounds = tu.ring_rounds ? tu.ring_rounds : 1;
     return true;
 }
 
-static cudaError_t ring_forward(const tp_desc *d, const RingLaunch &rl0, const void *x, const float *sh,
-                                const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src,
-                                int32_t N_dst, int64_t E, float *out, void *ws, size_t ws_bytes, int *status,
-                                cudaStream_t stream) {
-    RingLaunch rl = rl0;
-    const Tables &T = d->tab;
-    const int rounds = rl.n_pieces / rl.n_warps;
-    // a smaller caller workspace: fewer warps
-    while (rl.n_warps > 1 && carry_bytes(rl.n_warps * rounds, T.dim_out) > ws_bytes) rl.n_warps = (rl.n_warps + 1) / 2;
-    rl.n_pieces = rl.n_warps * rounds;
-    if (!ws || carry_bytes(rl.n_pieces, T.dim_out) > ws_bytes) return cudaErrorNotSupported;
-    static_assert(sizeof(RingParams) < 32000, "kernel parameter block too large");
-    RingParams prm;
-    std::memset(&prm, 0, sizeof(prm));
-    prm = rl.geo;
-    std::memcpy(prm.ej, d->prog.ej, sizeof(uint32_t) * d->prog.R);
-    std::memcpy(prm.ec, d->prog.ec, sizeof(float) * 2 * d->prog.R);
-    prm.x = x;
-    prm.sh = sh;
-    prm.w = w;
-    prm.src = src;
-    prm.row_ptr = row_ptr;
-    prm.out = out;
-    prm.carry = static_cast<float *>(ws);
-    const size_t cb = ((size_t)2 * rl.n_pieces * T.dim_out * sizeof(float) + 255) / 256 * 256;
-    prm.carry_dst = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(ws) + cb);
-    prm.status = status;
-    prm.n_src = N_src;
-    prm.n_dst = N_dst;
-    prm.n_warps = rl.n_warps;
-    prm.n_pieces = rl.n_pieces;
-    prm.E = E;
-    const int blocks = (rl.n_warps + rl.wpb - 1) / rl.wpb;
-    void *args[] = {&prm};
-    cudaError_t e = cudaLaunchKernel(rl.fn, dim3(blocks), dim3(32 * rl.wpb), args, (size_t)rl.smem, stream);
-    if (e != cudaSuccess) return e;
-    const int wpb = 8;
-    carry_fixup_kernel<<<(rl.n_pieces + wpb - 1) / wpb, 32 * wpb, 0, stream>>>(prm.carry, prm.carry_dst, rl.n_pieces,
-                                                                                T.dim_out, out);
-    return cudaGetLastError();
+// Plans are cached per (descriptor, device, dtype, tuning generation), so a
+// forward call makes no CUDA attribute or occupancy query after the first.
+namespace {
+struct PlanKey {
+    uint64_t uid;
+    int dev, dtype;
+    uint32_t gen;
+    bool operator<(const PlanKey &o) const {
+        return std::tie(uid, dev, dtype, gen) < std::tie(o.uid, o.dev, o.dtype, o.gen);
+    }
+};
+std::mutex g_plan_mu;
+std::map<PlanKey, std::unique_ptr<RingLaunch>> g_plans;  // nullptr: no ring kernel for this key
+}  // namespace
+
+void launch_cache_forget(uint64_t uid) {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    for (auto it = g_plans.begin(); it != g_plans.end();) it = it->first.uid == uid ? g_plans.erase(it) : std::next(it);
+}
+
+static const RingLaunch *cached_plan(const tp_desc *d, tp_dtype dtype, int dev, int smem_optin, const TuningState &ts) {
+    const PlanKey key{d->uid, dev, (int)dtype, ts.gen};
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) return it->second.get();
+    std::unique_ptr<RingLaunch> rl(new RingLaunch());
+    if (!ring_plan(d, dtype, smem_optin, ts.t, *rl)) rl.reset();
+    const RingLaunch *p = rl.get();
+    g_plans[key] = std::move(rl);
+    return p;
+}
+
+// Warps and pieces for E edges: every resident warp slot, but at least ~64
+// edges per warp.
+static void ring_geometry(const RingLaunch &rl, int64_t E, int sms, int &n_warps, int &n_pieces) {
+    long long nw = (long long)sms * rl.occ * rl.wpb;
+    const long long by_edges = (E + 63) / 64;
+    if (nw > by_edges) nw = by_edges;
+    if (nw < 1) nw = 1;
+    n_warps = (int)nw;
+    n_pieces = n_warps * rl.rounds;
 }
 
 // Workspace the split forward needs (0: this descriptor has no program kernel
 // or the input does not qualify).
-size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sms, int smem_optin) {
-    RingLaunch rl;
-    if (!ring_plan(d, dtype, E, sms, smem_optin, rl)) return 0;
-    return carry_bytes(rl.n_pieces, d->tab.dim_out);
+size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin) {
+    const TuningState ts = tuning_snapshot();
+    if (ts.t.disable_split || E >= (int64_t)1 << 31) return 0;
+    const RingLaunch *rl = cached_plan(d, dtype, dev, smem_optin, ts);
+    if (!rl) return 0;
+    int nw, np;
+    ring_geometry(*rl, E, sms, nw, np);
+    return carry_bytes(np, d->tab.dim_out);
 }
 
 // Launches the ring kernel (+ partial merge). Returns cudaErrorNotSupported
@@ -178,14 +173,48 @@ size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int sm
 // hold the partials (the caller then uses the generic kernel).
 cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
                           const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
-                          float *out, void *ws, size_t ws_bytes, int sms, int smem_optin, int *status,
+                          float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
                           cudaStream_t stream) {
-    if (env_int("TPCONV_DISABLE_SPLIT", 0)) return cudaErrorNotSupported;
-    RingLaunch rl;
+    const TuningState ts = tuning_snapshot();
+    if (ts.t.disable_split || !ws || E >= (int64_t)1 << 31) return cudaErrorNotSupported;  // 32-bit edge indices inside
     const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
                          reinterpret_cast<uintptr_t>(sh);
-    if ((al & 15u) != 0 || !ring_plan(d, dtype, E, sms, smem_optin, rl)) return cudaErrorNotSupported;
-    return ring_forward(d, rl, x, sh, w, src, row_ptr, N_src, N_dst, E, out, ws, ws_bytes, status, stream);
+    if ((al & 15u) != 0) return cudaErrorNotSupported;
+    const RingLaunch *rl = cached_plan(d, dtype, dev, smem_optin, ts);
+    if (!rl) return cudaErrorNotSupported;
+    const Tables &T = d->tab;
+    int n_warps, n_pieces;
+    ring_geometry(*rl, E, sms, n_warps, n_pieces);
+    // a smaller caller workspace: fewer warps
+    while (n_warps > 1 && carry_bytes(n_warps * rl->rounds, T.dim_out) > ws_bytes) n_warps = (n_warps + 1) / 2;
+    n_pieces = n_warps * rl->rounds;
+    if (carry_bytes(n_pieces, T.dim_out) > ws_bytes) return cudaErrorNotSupported;
+    static_assert(sizeof(RingParams) < 32000, "kernel parameter block too large");
+    RingParams prm = rl->geo;
+    prm.x = x;
+    prm.sh = sh;
+    prm.w = w;
+    prm.src = src;
+    prm.row_ptr = row_ptr;
+    prm.out = out;
+    prm.carry = static_cast<float *>(ws);
+    const size_t cb = ((size_t)2 * n_pieces * T.dim_out * sizeof(float) + 255) / 256 * 256;
+    prm.carry_dst = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(ws) + cb);
+    prm.status = status;
+    prm.n_src = N_src;
+    prm.n_dst = N_dst;
+    prm.n_warps = n_warps;
+    prm.n_pieces = n_pieces;
+    prm.E = E;
+    prm.wait_ns = ts.t.wait_limit_ns > 0 ? (uint64_t)ts.t.wait_limit_ns : kWaitNs;
+    const int blocks = (n_warps + rl->wpb - 1) / rl->wpb;
+    void *args[] = {&prm};
+    cudaError_t e = cudaLaunchKernel(rl->fn, dim3(blocks), dim3(32 * rl->wpb), args, (size_t)rl->smem, stream);
+    if (e != cudaSuccess) return e;
+    const int wpb = 8;
+    carry_fixup_kernel<<<(n_pieces + wpb - 1) / wpb, 32 * wpb, 0, stream>>>(prm.carry, prm.carry_dst, n_pieces,
+                                                                            T.dim_out, N_dst, out);
+    return cudaGetLastError();
 }
 
 }  // namespace tpc

@@ -56,7 +56,13 @@ struct ProgramPlan {
 
 }  // namespace tpc
 
+namespace tpc {
+// Drop the launch plans cached for descriptor `uid` (called when it is destroyed).
+void launch_cache_forget(uint64_t uid);
+}  // namespace tpc
+
 struct tp_desc {
+    uint64_t uid;  // unique per descriptor created in this process (launch-plan cache key)
     // parsed irreps: (mul, l, parity) with parity +1/-1 (O3) or 0 (SO3)
     int n_in, n_sh, n_out;
     int in_mul[8], in_l[8], in_p[8];

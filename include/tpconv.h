@@ -66,7 +66,8 @@ typedef enum {
     TP_OK = 0,
     TP_ERR_PARSE = 1,       /* an irreps string cannot be parsed */
     TP_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (see tp_desc_create) */
-    TP_ERR_UNSORTED = 3,    /* row pointers not non-decreasing / not ending at E */
+    /* 3 is unused: row pointers live in device memory and are checked by the
+       kernels, which report bad ones through TP_DEV_ERR_SEGMENT */
     TP_ERR_INDEX = 4,       /* an index is out of range */
     TP_ERR_ALIGN = 5,       /* a pointer or row size breaks the 16-byte rule */
     TP_ERR_CUDA = 6,        /* a CUDA runtime call failed */
@@ -84,7 +85,7 @@ typedef enum {
 
 /* device status bits (tp_device_status) */
 #define TP_DEV_ERR_INDEX 0x1   /* src/dst/key outside [0, N) - the edge was skipped */
-#define TP_DEV_ERR_TIMEOUT 0x2 /* an mbarrier wait exceeded its iteration limit */
+#define TP_DEV_ERR_TIMEOUT 0x2 /* a pipeline (mbarrier) wait exceeded its time limit; outputs unspecified */
 #define TP_DEV_ERR_SEGMENT 0x4 /* row pointers not non-decreasing or outside [0, E] */
 #define TP_DEV_ERR_INTERNAL 0x8 /* a kernel's own consistency check failed (a library bug); the access was skipped */
 
@@ -140,7 +141,11 @@ TPCONV_API tp_status tp_spherical_harmonics(const tp_desc *desc, const float *ve
 TPCONV_API tp_status tp_csr_workspace_size(int64_t E, int32_t N, size_t *bytes);
 
 /* Stable counting sort of keys (a dst-sorted CSR when keys = dst; a source
- * CSR for the backward when keys = src in dst-sorted edge order).
+ * CSR for the backward when keys = src in dst-sorted edge order). The
+ * destination-sorted edge list is what the gather/scatter of "cuEquivariance
+ * in PyTorch", SegmentedPolynomial: gather and scatter, sums over (one
+ * contiguous edge range per output row), and the same page's Limitations and
+ * backends notes that indexed kernels want sorted indices.
  * keys: device int32 [E] in [0, N). Outputs (device, caller-owned):
  *   perm[E]         perm[k] = original position of the k-th sorted key; equal
  *                   keys keep their original order;
@@ -153,28 +158,34 @@ TPCONV_API tp_status tp_csr_build(const int32_t *keys, int64_t E, int32_t N, int
                        int32_t *keys_sorted, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Allocation-free tp_csr_build. The pages have no counterpart: this entry
- * point exists for callers that must not allocate device memory at all, for
- * example a plugin's enqueue function or code running while a stream is being
- * captured into a CUDA graph (cudaMalloc is not allowed there, and elsewhere it
- * may synchronise the device), or a program whose device memory is entirely
- * owned by another allocator. Results are identical to tp_csr_build.
+ * point is for callers that cannot allocate device memory themselves, such as
+ * a plugin whose enqueue callback of a host framework receives only the
+ * tensors it reads and writes, or a program whose device memory is entirely
+ * owned by another allocator, where an extra cudaMalloc would fail, break the
+ * allocator's accounting, or synchronise the device. Results are identical to
+ * tp_csr_build.
  * The sort's scratch is a fixed array inside the library (about 3.3 MB, held on
  * every GPU that loads the library until the process exits); the caller still
  * passes keys and the outputs. E may be at most
  * tp_csr_build_noalloc_max_edges() (262144); larger E returns TP_ERR_CAPACITY
  * without launching anything. The first call on each device looks up the
  * array's device address (a one-time set-up, no allocation); make that first
- * call before capturing a stream. All calls share the one array, so calls that
- * overlap on the GPU (different streams, or different host threads) race and
- * must be serialised by the caller. Nothing in the array needs to start at
- * zero: every call overwrites what it reads. */
+ * call before any stream capture begins. All calls share the one array, so
+ * calls that overlap on the GPU (different streams, or different host
+ * threads) race and must be serialised by the caller. Nothing in the array
+ * needs to start at zero: every call overwrites what it reads. */
 TPCONV_API tp_status tp_csr_build_noalloc(const int32_t *keys, int64_t E, int32_t N, int32_t *perm,
                                           int32_t *row_ptr, int32_t *keys_sorted, void *stream);
 TPCONV_API int64_t tp_csr_build_noalloc_max_edges(void);
 
-/* Forward pass (the hot path). Edges must be in destination-sorted order with
- * row_ptr[N_dst+1] from tp_csr_build (edge range of destination d is
- * [row_ptr[d], row_ptr[d+1])).
+/* Forward pass (the hot path): the formula at the top of this file, that is
+ * the channelwise product "[ijk]·a[uv]·b[iu]·c[jv] -> D[kuv]" of Lesson 12a:
+ * Foundations of cuEquivariance, section 21.4, with x gathered by source and
+ * the result sum-scattered by destination ("cuEquivariance in PyTorch",
+ * SegmentedPolynomial: gather and scatter; one weight row per edge as in
+ * Layouts and weights), every path in one launch (Lesson 12a, section 21.1).
+ * Edges must be in destination-sorted order with row_ptr[N_dst+1] from
+ * tp_csr_build (edge range of destination d is [row_ptr[d], row_ptr[d+1])).
  *   x:   device [N_src][dim_x], float32 (TP_F32) or bfloat16 (TP_BF16_IN_F32_OUT), ir_mul;
  *   sh:  device float32 [E][dim_sh];
  *   w:   device [E][weight_numel], same type as x;
@@ -202,7 +213,9 @@ TPCONV_API tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
                                      size_t workspace_bytes, void *stream);
 
 /* Backward pass of tp_conv_forward (float32), the exact gradients of
- * <grad_out, out> with respect to x, w and sh:
+ * <grad_out, out> with respect to x, w and sh ("cuEquivariance in PyTorch",
+ * CPU tensor product and backward: gradients with respect to both inputs and
+ * the weights; the forward is linear in each of them, so these sums are exact):
  *   dx[s,a,i,u] = sum_{e: src[e]=s} sum_{p: a_p=a} w[e,p,u] sum_{j,k} C_p[i,j,k] sh[e,b,j] g[dst[e],c,k,u]
  *   dw[e,p,u]   = sum_{i,j,k} C_p[i,j,k] x[src[e],a,i,u] sh[e,b,j] g[dst[e],c,k,u]
  *   dsh[e,b,j]  = sum_{p: b_p=b} sum_{i,k,u} C_p[i,j,k] x[src[e],a,i,u] w[e,p,u] g[dst[e],c,k,u]
@@ -215,6 +228,33 @@ TPCONV_API tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out
                            const float *w, const int32_t *src, const int32_t *dst, const int32_t *row_ptr,
                            const int32_t *src_perm, const int32_t *src_row_ptr, int32_t N_src,
                            int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh, void *stream);
+
+/* Launch tuning and test hooks. The pages have no counterpart: these settings
+ * exist for tests and tuning sweeps, and normal use never needs them. They
+ * are process-wide and apply to calls made after tp_set_tuning returns; a zero
+ * field keeps the library's default.
+ *   ring_stage_bytes  target bytes per chunk of the forward's warp ring (>= 0)
+ *   ring_stages       stages per warp ring, 2..8
+ *   ring_warps        warps per block of the ring kernel, 1..8
+ *   ring_rounds       pieces of the edge list per warp, 1..16
+ *   ring_pack         1: packed two-lane FMAs, 2: plain FMAs
+ *   disable_split     1: the forward uses its generic per-destination kernel
+ *   wait_limit_ns     time after which a kernel's main-loop pipeline wait gives
+ *                     up and sets TP_DEV_ERR_TIMEOUT (default 1 s); waits that
+ *                     let a failed warp's copies land before it exits always
+ *                     keep the 1 s limit.
+ * tp_set_tuning(NULL) restores every default. TP_ERR_ARG for a field out of range. */
+typedef struct {
+    int32_t ring_stage_bytes;
+    int32_t ring_stages;
+    int32_t ring_warps;
+    int32_t ring_rounds;
+    int32_t ring_pack;
+    int32_t disable_split;
+    int64_t wait_limit_ns;
+} tp_tuning;
+TPCONV_API tp_status tp_set_tuning(const tp_tuning *tuning);
+TPCONV_API tp_status tp_get_tuning(tp_tuning *tuning);
 
 /* Read (and, when reset != 0, clear) the current device's status word into
  * *flags (TP_DEV_ERR_* bits). Synchronises `stream`. */

@@ -24,7 +24,7 @@ generators):
 * ``cref``     the same forward/backward as plain C loops with OpenMP, used for
                sizes the numpy version is too slow for and for the CPU baseline.
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open:
 real basis ordered m=-l..l with the z axis as pole and l=1 = sqrt(3)(y,z,x);
 "component" normalisation (sum_m Y_lm^2 = 2l+1 on the unit sphere);
 Clebsch-Gordan tensors orthonormal over (i,j) for each k with no extra path

@@ -74,3 +74,18 @@ def err(got, ref):
     if isinstance(got, torch.Tensor):
         got = got.detach().double().cpu().numpy()
     return tp.rms_rel_err(got, ref)
+
+
+class tuning:
+    """Context manager: tp_set_tuning(**fields) inside the block, defaults after."""
+
+    def __init__(self, tpc, **fields):
+        self.tpc, self.fields = tpc, fields
+
+    def __enter__(self):
+        self.tpc.tp_set_tuning(**self.fields)
+        return self
+
+    def __exit__(self, *exc):
+        self.tpc.tp_set_tuning()
+        return False

@@ -93,3 +93,29 @@ def test_backward_deterministic(tpc):
     b = run_backward(tpc, prob, g_np)
     for u, v in zip(a[:3], b[:3]):
         assert torch.equal(u, v)
+
+
+def test_backward_out_of_range_source_gives_zero_edge_rows(tpc):
+    """An edge whose source is out of range is skipped and flagged; its dw and
+    dsh rows are still written (as zeros), the other edges are unaffected."""
+    prob = make_problem(*SHAPES[1], n_src=64, n_dst=64, E=1500, seed=44)
+    g_np = np.random.default_rng(45).standard_normal((64, prob["plan"].dim_out))
+    desc = tpc.tp_desc_create(*prob["irreps"])
+    g = gpu_sorted_inputs(tpc, prob)
+    bad = g["src"].clone()
+    bad[100] = 64
+    sp, srp, _ = tpc.tp_csr_build(g["src"], prob["n_src"])
+    dw = torch.full((1500, desc.weight_numel), 7.0, device="cuda")
+    dsh = torch.full((1500, desc.dim_sh), 7.0, device="cuda")
+    tpc.tp_conv_backward(desc, dev_tensor(g_np), g["x"], g["sh"], g["w"], bad, g["dst"], g["row_ptr"], sp, srp,
+                         dw=dw, dsh=dsh)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) & tpc.TP_DEV_ERR_INDEX
+    assert not dw[100].any() and not dsh[100].any()
+    perm = g["perm"].cpu().numpy()
+    _, rdw, rdsh = oracle_backward(prob, g_np)
+    keep = np.ones(1500, bool)
+    keep[100] = False
+    assert err(dw[torch.as_tensor(keep, device="cuda")], rdw[perm][keep]) <= FP32_TOL
+    assert err(dsh[torch.as_tensor(keep, device="cuda")], rdsh[perm][keep]) <= FP32_TOL
+    assert tpc.tp_device_status(reset=True) == 0

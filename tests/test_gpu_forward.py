@@ -7,8 +7,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import deg_tol, BF16_TOL, FP32_TOL, dev_tensor, err, gpu_sorted_inputs, make_problem, oracle_forward
-from oracle import tp
+from helpers import deg_tol, BF16_TOL, FP32_TOL, dev_tensor, err, gpu_sorted_inputs, make_problem, oracle_forward, tuning
+from oracle import cref, so3, tp
 from workloads import WORKLOADS, make_features, make_graph
 
 pytestmark = pytest.mark.gpu
@@ -128,32 +128,31 @@ def test_split_kernel_default_geometry(tpc, irr, dtype):
 
 
 RING_GEOMETRIES = {
-    "eps1-S2-w1": {"TPCONV_RING_STAGE_BYTES": "1", "TPCONV_RING_STAGES": "2", "TPCONV_RING_WARPS": "1"},
-    "eps30-S3": {"TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_STAGES": "3"},
-    "S8-w8": {"TPCONV_RING_STAGES": "8", "TPCONV_RING_WARPS": "8", "TPCONV_RING_STAGE_BYTES": "4096"},
-    "rounds3": {"TPCONV_RING_ROUNDS": "3"},
-    "rounds16-eps5": {"TPCONV_RING_ROUNDS": "16", "TPCONV_RING_STAGE_BYTES": "5000"},
-    "eps30-pack": {"TPCONV_RING_STAGE_BYTES": "1000000", "TPCONV_RING_PACK": "1"},
-    "nopack": {"TPCONV_RING_PACK": "0"},
-    "rounds4-S4": {"TPCONV_RING_ROUNDS": "4", "TPCONV_RING_STAGES": "4"},
+    "eps1-S2-w1": dict(ring_stage_bytes=1, ring_stages=2, ring_warps=1),
+    "eps30-S3": dict(ring_stage_bytes=1000000, ring_stages=3),
+    "S8-w8": dict(ring_stages=8, ring_warps=8, ring_stage_bytes=4096),
+    "rounds3": dict(ring_rounds=3),
+    "rounds16-eps5": dict(ring_rounds=16, ring_stage_bytes=5000),
+    "eps30-pack": dict(ring_stage_bytes=1000000, ring_pack=1),
+    "nopack": dict(ring_pack=2),
+    "rounds4-S4": dict(ring_rounds=4, ring_stages=4),
 }
 
 
 @pytest.mark.parametrize("geo", list(RING_GEOMETRIES))
 @pytest.mark.parametrize("irr,dtype", [(SHAPES[0], torch.float32), (SHAPES[1], torch.float32),
                                        (SHAPES[2], torch.bfloat16)], ids=["cpt1", "cpt4", "cpt2-bf16"])
-def test_ring_geometries(tpc, monkeypatch, irr, dtype, geo):
+def test_ring_geometries(tpc, irr, dtype, geo):
     """The warp ring with chunks of 1 to 30 edges, 2 to 8 stages, 1 to 8 warps
     per block, several pieces per warp, packed or scalar FMAs, on a graph with a 1000-edge
     destination (cut across many pieces), empty destinations and a ragged tail."""
-    for k, v in RING_GEOMETRIES[geo].items():
-        monkeypatch.setenv(k, v)
     rng = np.random.default_rng(21)
     n_dst = 500
     dst = np.concatenate([np.full(1000, 7), rng.integers(0, n_dst // 2, 5003) * 2, [n_dst - 1]])
     rng.shuffle(dst)
     prob = make_problem(*irr, n_src=300, n_dst=n_dst, E=len(dst), seed=22, dst=dst)
-    out, _, _ = run(tpc, prob, dtype)
+    with tuning(tpc, **RING_GEOMETRIES[geo]):
+        out, _, _ = run(tpc, prob, dtype)
     ref = oracle_forward(prob, dtype)
     on = out.double().cpu().numpy()
     for d, c in zip(*np.unique(dst, return_counts=True)):
@@ -211,3 +210,56 @@ def test_bad_row_pointers_flagged(tpc):
     tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], rp, 64)
     torch.cuda.synchronize()
     assert tpc.tp_device_status(reset=True) & tpc.TP_DEV_ERR_SEGMENT
+
+
+@pytest.mark.parametrize("mode", ["split", "generic"])
+def test_wait_timeout_is_reported_and_writes_stay_in_bounds(tpc, mode):
+    """A main-loop wait limit of 1 ns (tp_set_tuning) makes pipeline waits give
+    up on real chunks whose copies are still in flight; every copy still lands,
+    because the waits after a failure keep the full limit. The call returns,
+    TP_DEV_ERR_TIMEOUT is reported, no byte outside `out` changes (guard rows
+    around it keep their sentinel) although the split kernel runs several pieces
+    per warp, and the next call with default settings is correct again."""
+    irr = SHAPES[1]
+    plan = tp.Plan(*irr)
+    n, E = 4096, 100000
+    rng = np.random.default_rng(50)
+    dst = np.sort(rng.integers(0, n, E))
+    src = rng.integers(0, n, E)
+    x = rng.standard_normal((n, plan.dim_in), dtype=np.float32)
+    w = rng.standard_normal((E, plan.weight_numel), dtype=np.float32)
+    vec = rng.standard_normal((E, 3))
+    sh = so3.sh_concat([t.l for t in plan.irr_sh], vec)
+    desc = tpc.tp_desc_create(*irr)
+    d_x, d_w, d_sh = dev_tensor(x), dev_tensor(w), dev_tensor(sh)
+    d_src = dev_tensor(src, torch.int32)
+    _, row_ptr, _ = tpc.tp_csr_build(dev_tensor(dst, torch.int32), n)
+    guard = 97
+    big = torch.full((n + 2 * guard, desc.dim_out), 12345.0, device="cuda")
+    out = big[guard:guard + n]
+    fields = dict(wait_limit_ns=1, ring_rounds=4) if mode == "split" else dict(wait_limit_ns=1, disable_split=1)
+    hit = False
+    for _ in range(3):
+        with tuning(tpc, **fields):
+            tpc.tp_conv_forward(desc, d_x, d_sh, d_w, d_src, row_ptr, n, out=out)
+            torch.cuda.synchronize()
+        st = tpc.tp_device_status(reset=True)
+        assert st & ~tpc.TP_DEV_ERR_TIMEOUT == 0
+        assert torch.all(big[:guard] == 12345.0) and torch.all(big[guard + n:] == 12345.0)
+        hit = hit or bool(st & tpc.TP_DEV_ERR_TIMEOUT)
+        if hit:
+            break
+    assert hit, "no pipeline wait ran out under a 1 ns limit"
+    again = tpc.tp_conv_forward(desc, d_x, d_sh, d_w, d_src, row_ptr, n)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+    rows = np.array([0, 1, 2, 777, 2048, n - 1])
+    rp = np.zeros(n + 1, dtype=np.int64)
+    np.cumsum(np.bincount(dst, minlength=n), out=rp[1:])
+    sel = np.concatenate([np.arange(rp[r], rp[r + 1]) for r in rows])
+    lrp = np.zeros(len(rows) + 1, dtype=np.int64)
+    np.cumsum(rp[rows + 1] - rp[rows], out=lrp[1:])
+    sh32 = sh.astype(np.float32).astype(np.float64)
+    ref = cref.conv_forward(plan, x.astype(np.float64), sh32[sel], w[sel].astype(np.float64), src[sel], lrp,
+                            len(rows))
+    assert err(again[torch.as_tensor(rows, device="cuda")], ref) <= FP32_TOL

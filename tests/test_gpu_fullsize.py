@@ -33,7 +33,7 @@ def test_fullsize_sampled_rows(tpc, name):
     import bench
     dev = torch.device("cuda:0")
     wl, desc, inp, n, E, host = bench.build_inputs(name, 0, tpc, torch, dev)
-    x, w, src, dst, vec = host
+    x, w, src, dst, vec, _ = host
     out = tpc.tp_conv_forward(desc, inp["x"], inp["sh"], inp["w"], inp["src"], inp["row_ptr"], n)
     torch.cuda.synchronize()
     assert tpc.tp_device_status(reset=True) == 0
@@ -61,3 +61,46 @@ def test_fullsize_sampled_rows(tpc, name):
             assert err(g, r) <= deg_tol(int(d))
         else:
             assert not np.any(g)
+
+
+def test_backward_fwdbwd_fullsize(tpc):
+    """The backward of the fwd+bwd configuration at its full size (the medium
+    graph, N=4096, E=131064, 13 paths, mul 128, with its own grad_out), run
+    exactly as bench.py times it, checked on samples the fp64 C oracle
+    recomputes from the host copies: about 50 dx rows (random ones, the first,
+    the last and the source with the most edges) through the oracle's own
+    source CSR, and about 2000 edges of dw and dsh."""
+    import bench
+    dev = torch.device("cuda:0")
+    wl, desc, inp, n, E, host = bench.build_inputs("fwdbwd", 0, tpc, torch, dev)
+    x, w, src, dst, vec, g = host
+    go, dst_d, sp, srp = bench.backward_inputs(tpc, torch, inp, n, g)
+    dx, dw, dsh = tpc.tp_conv_backward(desc, go, inp["x"], inp["sh"], inp["w"], inp["src"], dst_d, inp["row_ptr"],
+                                       sp, srp)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+
+    plan = tp.Plan(wl.irreps_in, wl.irreps_sh, wl.irreps_out)
+    order = np.argsort(dst, kind="stable")           # the oracle's own destination sort
+    src_s, dst_s = src[order], dst[order]
+    sh_s = so3.sh_concat([t.l for t in plan.irr_sh], vec[order].astype(np.float32).astype(np.float64))
+    x64, w_s, g64 = x.astype(np.float64), w[order].astype(np.float64), g.astype(np.float64)
+    rng = np.random.default_rng(321)
+
+    edges = np.unique(np.concatenate([rng.choice(E, 2000, replace=False), [0, E - 1]]))
+    rdw, rdsh = cref.conv_backward_edges(plan, x64, sh_s, w_s, g64, src_s, dst_s, edges=edges)
+    ed = torch.as_tensor(edges, device=dev)
+    assert err(dw[ed], rdw) <= FP32_TOL
+    assert err(dsh[ed], rdsh) <= FP32_TOL
+
+    sp_o, srp_o, _ = tp.csr_build(src_s, n)
+    outdeg = np.diff(srp_o)
+    rows = np.unique(np.concatenate([rng.choice(n, 48, replace=False), [0, n - 1, int(np.argmax(outdeg))]]))
+    rdx = cref.conv_backward_dx(plan, sh_s, w_s, g64, dst_s, sp_o, srp_o, n, rows=rows)
+    got = dx[torch.as_tensor(rows, device=dev)].double().cpu().numpy()
+    assert err(got, rdx) <= FP32_TOL
+    for gr, rr, d in zip(got, rdx, outdeg[rows]):
+        if d:
+            assert err(gr, rr) <= deg_tol(int(d))
+        else:
+            assert not np.any(gr)

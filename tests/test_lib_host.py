@@ -100,3 +100,20 @@ def test_argument_errors_need_no_gpu(tpc):
     assert lib.tp_csr_build(good, 1000, 50, good, good, vp(0), good, 16, vp(0)) == 7
     assert lib.tp_csr_build(good, 1000, 50, good, good, vp(0), vp(0x10010), n.value, vp(0)) == 5
     assert lib.tp_csr_build(good, 10, 0, good, good, vp(0), good, n.value, vp(0)) == 4
+
+
+def test_tuning_hooks_validate_and_reset(tpc):
+    """tp_set_tuning stores in-range settings, rejects out-of-range ones with
+    TP_ERR_ARG (leaving the previous settings), and NULL restores defaults."""
+    assert tpc.tp_get_tuning() == {f: 0 for f in tpc.TUNING_FIELDS}
+    tpc.tp_set_tuning(ring_stages=3, ring_rounds=4, wait_limit_ns=5)
+    got = tpc.tp_get_tuning()
+    assert (got["ring_stages"], got["ring_rounds"], got["wait_limit_ns"], got["ring_warps"]) == (3, 4, 5, 0)
+    for bad in (dict(ring_stages=1), dict(ring_stages=9), dict(ring_warps=9), dict(ring_rounds=17),
+                dict(ring_pack=3), dict(disable_split=2), dict(wait_limit_ns=-1), dict(ring_stage_bytes=-4)):
+        with pytest.raises(tpc.TPError) as ei:
+            tpc.tp_set_tuning(**bad)
+        assert tpc.STATUS_NAMES[ei.value.status] == "TP_ERR_ARG"
+    assert tpc.tp_get_tuning()["ring_rounds"] == 4
+    tpc.tp_set_tuning()
+    assert tpc.tp_get_tuning() == {f: 0 for f in tpc.TUNING_FIELDS}

@@ -4,6 +4,7 @@ versions, scatter semantics, rotation and inversion equivariance, layout
 invariance, exact adjoint identities and finite differences, and the stable
 counting sort."""
 import json
+import math
 import os
 
 import numpy as np
@@ -253,3 +254,23 @@ def test_workload_generator_shapes():
     assert np.all(np.diff(dst) >= 0) and np.all(src != dst)
     assert 120_000 < len(src) < 142_000
     assert np.all(np.linalg.norm(vec, axis=1) < 5.0)
+
+
+def test_rms_rel_err_hand_computed():
+    """The error measure every GPU parity assertion divides by, pinned to
+    values worked out by hand: max |got - ref| over the tensor, divided by the
+    root mean square of the reference (not of `got`, not a mean error)."""
+    # ref = [3, 4]: RMS = sqrt((9 + 16) / 2) = sqrt(12.5); largest difference 1
+    assert tp.rms_rel_err(np.array([3.0, 5.0]), np.array([3.0, 4.0])) == pytest.approx(1.0 / math.sqrt(12.5),
+                                                                                       rel=1e-15)
+    # the maximum, not the mean, of the differences: |[0.5, -2, 0]| -> 2; RMS of ref = 2
+    assert tp.rms_rel_err(np.array([2.5, 0.0, 2.0]), np.array([2.0, 2.0, 2.0])) == pytest.approx(1.0, rel=1e-15)
+    # the reference's RMS, not got's: swapping the arguments changes the value
+    assert tp.rms_rel_err(np.array([3.0, 4.0]), np.array([3.0, 5.0])) == pytest.approx(1.0 / math.sqrt(17.0),
+                                                                                       rel=1e-15)
+    # 2-D tensors use every element
+    ref = np.array([[1.0, -1.0], [1.0, -1.0]])
+    assert tp.rms_rel_err(ref + np.array([[0.0, 0.0], [0.0, 0.25]]), ref) == pytest.approx(0.25, rel=1e-15)
+    # an all-zero reference: the plain max difference; an empty tensor: 0
+    assert tp.rms_rel_err(np.array([0.0, -0.5]), np.zeros(2)) == 0.5
+    assert tp.rms_rel_err(np.zeros((0, 4)), np.zeros((0, 4))) == 0.0

@@ -1,19 +1,22 @@
 """tp_csr_build_noalloc: the CSR builder for callers that cannot allocate
-device memory (for example code that runs while a stream is being captured
-into a CUDA graph, or a plugin's enqueue function, where cudaMalloc is not
-allowed, or a program whose device memory belongs to another allocator).
+device memory themselves (a plugin's enqueue callback that is handed only the
+tensors it reads and writes, or a program whose device memory belongs to
+another allocator).
 
 It is called here through the C ABI with caller-owned outputs only, twice in a
 row, and must give exactly what tp_csr_build (which takes a caller workspace)
-gives - the sort is integer work, so "within the tests' tolerance" means
-bit-exact. The file is named to be collected last; it passes on its own in a
-fresh process as well as after the other tests.
+gives, and exactly the oracle's stable counting sort - the sort is integer
+work, so "within the tests' tolerance" means bit-exact. The file is named to be
+collected last; it passes on its own in a fresh process as well as after the
+other tests.
 """
 import ctypes
 
 import numpy as np
 import pytest
 import torch
+
+from oracle import tp
 
 pytestmark = pytest.mark.gpu
 
@@ -37,10 +40,12 @@ def test_noalloc_matches_workspace_entry_point(tpc, E, N):
     keys = torch.as_tensor(rng.integers(0, N, E).astype(np.int32)).cuda()
     ref = tpc.tp_csr_build(keys, N)
     torch.cuda.synchronize()
+    oracle = tp.csr_build(keys.cpu().numpy(), N)
     for _ in range(2):   # the scratch array keeps the previous call's contents
         got = _call_noalloc(tpc, keys, N)
-        for a, b in zip(got, ref):
+        for a, b, c in zip(got, ref, oracle):
             assert torch.equal(a, b)
+            assert np.array_equal(a.cpu().numpy(), c)
     assert tpc.tp_device_status(reset=True) == 0
 
 

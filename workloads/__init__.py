@@ -18,11 +18,13 @@ convolution this library implements):
 * ``fd``        16 nodes, 64 uniform random edges (finite-difference checks).
 
 Random draws use ``numpy.random.default_rng([seed, workload_id])`` in the fixed
-order graph -> edge vectors -> x -> w -> grad_out, all in float64.
+order graph -> edge vectors -> x -> w -> grad_out (w in blocks of 65536 rows,
+each block from a generator seeded by the next draw of the stream).
 """
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -154,14 +156,34 @@ def make_graph(w: Workload, seed: int = 0):
     return rng, src, dst, vec, n
 
 
+def _normal_rows(rng: np.random.Generator, rows: int, cols: int, dtype, chunk: int = 65536) -> np.ndarray:
+    """[rows, cols] N(0,1) draws. Blocks of ``chunk`` rows each come from their
+    own generator, seeded by one draw from ``rng`` per block, and are filled on
+    several threads (the full-size weight streams hold up to 3e9 values)."""
+    from concurrent.futures import ThreadPoolExecutor
+    n_blocks = (rows + chunk - 1) // chunk
+    seeds = rng.integers(0, 2 ** 63, size=n_blocks)
+    out = np.empty((rows, cols), dtype=dtype)
+
+    def fill(i):
+        lo, hi = i * chunk, min(rows, (i + 1) * chunk)
+        np.random.default_rng(int(seeds[i])).standard_normal((hi - lo, cols), dtype=dtype, out=out[lo:hi])
+
+    if n_blocks:
+        with ThreadPoolExecutor(max(1, min(16, n_blocks, os.cpu_count() or 1))) as ex:
+            list(ex.map(fill, range(n_blocks)))
+    return out
+
+
 def make_features(rng: np.random.Generator, w: Workload, n_nodes: int, n_edges: int,
                   dim_x: int, weight_numel: int, n_paths: int, dim_out: int, dtype=np.float64):
     """Draw x [N, dim_x], w [E, weight_numel] and (for backward workloads)
-    grad_out [N, dim_out], continuing ``rng``. ``dtype`` float64 (default) or
-    float32; the full-size workloads use float32 draws so the weight stream
-    (up to 1.9e9 values) fits in host memory."""
+    grad_out [N, dim_out], continuing ``rng`` (w in blocks of rows, see
+    ``_normal_rows``). ``dtype`` float64 (default) or float32; the full-size
+    workloads use float32 draws so the weight stream (up to 1.9e9 values)
+    fits in host memory."""
     x = rng.standard_normal((n_nodes, dim_x), dtype=dtype)
-    wt = rng.standard_normal((n_edges, weight_numel), dtype=dtype)
+    wt = _normal_rows(rng, n_edges, weight_numel, dtype)
     if w.w_scale == "inv_sqrt_paths":
         wt *= dtype(1.0 / math.sqrt(n_paths))
     g = rng.standard_normal((n_nodes, dim_out), dtype=dtype) if w.backward else None
