@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="xlarge", choices=["tiny", "medium", "large", "xlarge"])
-    ap.add_argument("--configs", default="medium,large,tiny",
+    ap.add_argument("--configs", default="medium,large,tiny,xlarge_vec,medium_vec",
                     help="other workloads timed into the same line (comma list; empty for none)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -184,6 +184,7 @@ def build_inputs(wname: str, seed: int, tpc, torch, device):
         src=torch.as_tensor(src).to(device)[p].contiguous(),
         row_ptr=row_ptr,
     )
+    inputs["vec"] = d_vec      # destination-sorted edge vectors (tp_conv_forward_vec)
     torch.cuda.synchronize()
     return wl, desc, inputs, n, E, (x, w, src, dst, vec, g)
 
@@ -204,10 +205,12 @@ def describe(wl, n, E):
     return f"{wl.name}: N={n} E={E} {wl.irreps_in} x {wl.irreps_sh} -> {wl.irreps_out} ({wl.dtype})"
 
 
-def algorithmic_bytes(desc, n, E, esz):
-    """Compulsory bytes of one forward: w, sh, src, one read of x, one write of
-    out, row pointers."""
-    return (E * desc.weight_numel * esz + E * desc.dim_sh * 4 + E * 4 + n * desc.dim_x * esz
+def algorithmic_bytes(desc, n, E, esz, from_vectors=False):
+    """Compulsory bytes of one forward: w, sh (or the 12-byte edge vectors when
+    the harmonics are evaluated in the kernel), src, one read of x, one write
+    of out, row pointers."""
+    per_edge_h = 12 if from_vectors else desc.dim_sh * 4
+    return (E * desc.weight_numel * esz + E * per_edge_h + E * 4 + n * desc.dim_x * esz
             + n * desc.dim_out * 4 + (n + 1) * 4)
 
 
@@ -251,11 +254,15 @@ def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 10
 
 
 class Forward:
-    """One workload's inputs on the device and its forward call."""
+    """One workload's inputs on the device and its forward call; with
+    `from_vectors` the call is tp_conv_forward_vec (harmonics evaluated in the
+    kernel from the 12-byte edge vectors)."""
 
-    def __init__(self, wname, seed, tpc, torch, device, stream):
+    def __init__(self, wname, seed, tpc, torch, device, stream, from_vectors=False):
         self.tpc, self.torch, self.stream = tpc, torch, stream
         self.wl, self.desc, self.inp, self.n, self.E, self.host = build_inputs(wname, seed, tpc, torch, device)
+        self.vec = self.inp.pop("vec")
+        self.from_vectors = from_vectors
         self.esz = 2 if self.wl.dtype == "bf16" else 4
         self.out = torch.empty((self.n, self.desc.dim_out), dtype=torch.float32, device=device)
         fdt = tpc.TP_BF16_IN_F32_OUT if self.wl.dtype == "bf16" else tpc.TP_F32
@@ -263,12 +270,16 @@ class Forward:
         self.ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device) if ws_bytes else None
         # the warp-ring kernel + its partial-row merge, or the generic kernel alone
         self.launches_per_step = 2 if ws_bytes else 1
-        self.abytes = algorithmic_bytes(self.desc, self.n, self.E, self.esz)
+        self.abytes = algorithmic_bytes(self.desc, self.n, self.E, self.esz, from_vectors)
 
     def step(self):
         i = self.inp
-        self.tpc.tp_conv_forward(self.desc, i["x"], i["sh"], i["w"], i["src"], i["row_ptr"], self.n, out=self.out,
-                                 workspace=self.ws, stream=self.stream)
+        if self.from_vectors:
+            self.tpc.tp_conv_forward_vec(self.desc, i["x"], self.vec, i["w"], i["src"], i["row_ptr"], self.n,
+                                         out=self.out, workspace=self.ws, stream=self.stream)
+        else:
+            self.tpc.tp_conv_forward(self.desc, i["x"], i["sh"], i["w"], i["src"], i["row_ptr"], self.n, out=self.out,
+                                     workspace=self.ws, stream=self.stream)
 
     def timed(self, steps, warmup, local, world=1, device=None):
         """CUDA-event time of `steps` back-to-back steps (ms, max over ranks)
@@ -306,7 +317,7 @@ class Forward:
                 "peak_source": peak_src}
 
     def describe(self):
-        return describe(self.wl, self.n, self.E)
+        return describe(self.wl, self.n, self.E) + (", harmonics from edge vectors" if self.from_vectors else "")
 
     def e2e(self, steps):
         """The same forward through the public call with the inputs in pinned
@@ -491,8 +502,9 @@ def bench_ours(args):
             if name == "tiny":
                 cfgs["tiny"] = tiny_latency(tpc, torch, device, stream)
                 continue
-            g = Forward(name, args.seed, tpc, torch, device, stream)
-            k = DEFAULT_STEPS[name]
+            base = name[:-4] if name.endswith("_vec") else name
+            g = Forward(base, args.seed, tpc, torch, device, stream, from_vectors=name.endswith("_vec"))
+            k = DEFAULT_STEPS[base]
             _, ms_c, clk = g.timed(k, warmup, local)
             cfgs[name] = {"workload": g.describe(), "value": g.E * k / (ms_c / 1e3), "unit": "edges/s",
                           "steps": k, "kernel_us": ms_c / k * 1e3,

@@ -40,6 +40,7 @@ TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
 EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
            "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
            "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
+           "tp_conv_forward_vec",
            "tp_conv_backward", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
            "tp_abi_version"]
 
@@ -60,7 +61,7 @@ class _Info(ctypes.Structure):
 class _Tuning(ctypes.Structure):
     _fields_ = [("ring_stage_bytes", ctypes.c_int32), ("ring_stages", ctypes.c_int32), ("ring_warps", ctypes.c_int32),
                 ("ring_rounds", ctypes.c_int32), ("ring_pack", ctypes.c_int32), ("disable_split", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_int64)]
+                ("wait_limit_ns", ctypes.c_int64), ("disable_mma", ctypes.c_int32), ("mma_stages", ctypes.c_int32)]
 
 
 class _Path(ctypes.Structure):
@@ -79,6 +80,7 @@ _sigs = {
     "tp_csr_build_noalloc": [_vp, _i64, _i32, _vp, _vp, _vp, _vp],
     "tp_conv_forward_workspace_size": [_vp, ctypes.c_int, _i32, _i64, ctypes.POINTER(_sz)],
     "tp_conv_forward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _sz, _vp],
+    "tp_conv_forward_vec": [_vp, ctypes.c_int, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _sz, _vp],
     "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
     "tp_set_tuning": [ctypes.POINTER(_Tuning)],
@@ -291,6 +293,29 @@ def tp_conv_forward(desc: Descriptor, x, sh, w, src, row_ptr, n_dst: int, out=No
                                 _dev_ptr(row_ptr, "row_ptr", torch.int32, 1), x.shape[0], n_dst, E,
                                 _dev_ptr(out, "out", torch.float32, 2), ws_ptr, ws_n, _stream(stream)),
            "tp_conv_forward")
+    return out
+
+
+def tp_conv_forward_vec(desc: Descriptor, x, vec, w, src, row_ptr, n_dst: int, normalize: bool = True, out=None,
+                        workspace="auto", stream=None):
+    """tp_conv_forward with the harmonics evaluated in the kernel from edge
+    vectors vec [E, 3] float32 (destination-sorted edge order)."""
+    torch = _torch()
+    dtype = _fwd_dtype(x, w)
+    E = src.shape[0]
+    if out is None:
+        out = torch.empty((n_dst, desc.dim_out), dtype=torch.float32, device=x.device)
+    if isinstance(workspace, str):
+        nb = tp_conv_forward_workspace_size(desc, dtype, n_dst, E)
+        workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_n = workspace.numel() if workspace is not None else 0
+    _check(_lib.tp_conv_forward_vec(desc.handle, dtype, _dev_ptr(x, "x", None, 2),
+                                    _dev_ptr(vec, "vec", torch.float32, 2), int(bool(normalize)),
+                                    _dev_ptr(w, "w", None, 2), _dev_ptr(src, "src", torch.int32, 1),
+                                    _dev_ptr(row_ptr, "row_ptr", torch.int32, 1), x.shape[0], n_dst, E,
+                                    _dev_ptr(out, "out", torch.float32, 2), ws_ptr, ws_n, _stream(stream)),
+           "tp_conv_forward_vec")
     return out
 
 

@@ -20,10 +20,15 @@ cudaError_t sh_launch(const float *vec, int64_t E, int normalize, const Tables &
 int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
 size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
-cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
-                         const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
-                         float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
-                         cudaStream_t stream);
+size_t mma_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
+cudaError_t mma_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
+                        const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
+                        float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
+                        cudaStream_t stream);
+cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, int vec_mode,
+                          const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
+                          int64_t E, float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin,
+                          int *status, cudaStream_t stream);
 
 // ---- process-wide tuning (tp_set_tuning) ----
 static std::mutex g_tune_mu;
@@ -194,7 +199,9 @@ extern "C" tp_status tp_conv_forward_workspace_size(const tp_desc *desc, tp_dtyp
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
-    *bytes = split_workspace_bytes(desc, dtype, E, dev.dev, dev.sms, dev.smem_optin);
+    const size_t a = split_workspace_bytes(desc, dtype, E, dev.dev, dev.sms, dev.smem_optin);
+    const size_t b = mma_workspace_bytes(desc, dtype, E, dev.dev, dev.sms, dev.smem_optin);
+    *bytes = a > b ? a : b;
     return TP_OK;
 }
 
@@ -218,7 +225,13 @@ extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
         DevInfo dev;
         tp_status st = dev_info(dev);
         if (st != TP_OK) return st;
-        const cudaError_t e = split_forward(desc, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, workspace,
+        // bfloat16 inputs: the tensor-core kernel first
+        cudaError_t e = mma_forward(desc, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, workspace,
+                                    workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
+                                    static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) return TP_OK;
+        if (e != cudaErrorNotSupported) return TP_ERR_CUDA;
+        e = split_forward(desc, dtype, x, sh, 0, w, src, row_ptr, N_src, N_dst, E, out, workspace,
                                            workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
                                            static_cast<cudaStream_t>(stream));
         if (e == cudaSuccess) return TP_OK;
@@ -250,6 +263,33 @@ extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
     prm.n_gather = N_src;
     prm.n_edges = E;
     return launch_seg(fn, prm, grid, warps, smem, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_conv_forward_vec(const tp_desc *desc, tp_dtype dtype, const void *x, const float *vec,
+                                         int32_t normalize, const void *w, const int32_t *src, const int32_t *row_ptr,
+                                         int32_t N_src, int32_t N_dst, int64_t E, float *out, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+    if (!desc || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
+    if (N_dst == 0) return TP_OK;
+    if (!out || !row_ptr) return TP_ERR_ARG;
+    if (E > 0 && (!x || !vec || !w || !src)) return TP_ERR_ARG;
+    if (E > 0 && N_src == 0) return TP_ERR_INDEX;
+    const Tables &T = desc->tab;
+    const int esz = dtype == TP_F32 ? 4 : 2;
+    if (((T.dim_x * esz) & 15) || ((T.wnum * esz) & 15)) return TP_ERR_ALIGN;
+    if (!aligned16(out) || (E > 0 && (!aligned16(x) || !aligned16(w) || !aligned16(vec) || !aligned4(src))))
+        return TP_ERR_ALIGN;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP_ERR_ALIGN;
+    DevInfo dev;
+    tp_status st = dev_info(dev);
+    if (st != TP_OK) return st;
+    const cudaError_t e = split_forward(desc, dtype, x, vec, normalize ? 1 : 2, w, src, row_ptr, N_src, N_dst, E, out,
+                                       workspace, workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
+                                       static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) return TP_OK;
+    (void)cudaGetLastError();
+    return e == cudaErrorNotSupported ? TP_ERR_UNSUPPORTED : TP_ERR_CUDA;
 }
 
 extern "C" tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out, const float *x, const float *sh,
@@ -333,7 +373,8 @@ extern "C" tp_status tp_set_tuning(const tp_tuning *t) {
                         (v.ring_warps == 0 || (v.ring_warps >= 1 && v.ring_warps <= kRingMaxWarps)) &&
                         (v.ring_rounds == 0 || (v.ring_rounds >= 1 && v.ring_rounds <= kRingMaxPiecesPerWarp)) &&
                         v.ring_pack >= 0 && v.ring_pack <= 2 && (v.disable_split == 0 || v.disable_split == 1) &&
-                        v.wait_limit_ns >= 0;
+                        v.wait_limit_ns >= 0 && (v.disable_mma == 0 || v.disable_mma == 1) &&
+                        (v.mma_stages == 0 || (v.mma_stages >= 3 && v.mma_stages <= 8));
         if (!ok) return TP_ERR_ARG;
     }
     std::lock_guard<std::mutex> lk(g_tune_mu);

@@ -79,15 +79,36 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
     return ok != 0;
 }
 
+// Non-blocking probe: true when the phase with this parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: true when the phase completed, false once about `limit_ns`
 // have passed since the first probe found it incomplete. The clock is read
-// only on that slow path, after every suspended probe.
+// only on that slow path, after every suspended probe. (A try_wait probe may
+// itself suspend for a system-dependent time, so limits under 2 us use
+// non-blocking probes instead.)
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
+    if (limit_ns < 2000u) {
+        const uint64_t t0 = global_ns();
+        for (;;) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (global_ns() - t0 > limit_ns) return false;
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    const uint32_t hint = limit_ns < 2000u ? (uint32_t)limit_ns : 2000u;
     for (;;) {
-        if (mbar_try_wait_hint(bar, parity, hint)) return true;
+        if (mbar_try_wait_hint(bar, parity, 2000u)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
 }
@@ -203,6 +224,58 @@ __device__ __forceinline__ void store_vec(float *p, const float (&v)[CPT]) {
     } else {
 #pragma unroll
         for (int c = 0; c < CPT; ++c) p[c] = v[c];
+    }
+}
+
+// Real spherical harmonics of degrees 0..L (L <= 3) of (x, y, z) into
+// Y[l*l + m + l], "component" normalisation, real basis m = -l..l with z as
+// pole and no Condon-Shortley sign ("cuEquivariance in PyTorch", Spherical
+// harmonics and a NumPy reference). With `unit` the vector is first scaled
+// to unit length (a zero vector gives Y_0 = 1 and zeros); otherwise these are
+// the raw homogeneous polynomials. The polynomials are the Cartesian forms of
+// the real harmonics times sqrt(4 pi):
+//   l=1: sqrt(3) (y, z, x)
+//   l=2: sqrt(15) xy, sqrt(15) yz, sqrt(5)/2 (2z^2-x^2-y^2), sqrt(15) xz, sqrt(15)/2 (x^2-y^2)
+//   l=3: sqrt(70)/4 y(3x^2-y^2), sqrt(105) xyz, sqrt(42)/4 y(4z^2-x^2-y^2),
+//        sqrt(7)/2 z(2z^2-3x^2-3y^2), sqrt(42)/4 x(4z^2-x^2-y^2),
+//        sqrt(105)/2 z(x^2-y^2), sqrt(70)/4 x(x^2-3y^2)
+template <int L>
+__device__ __forceinline__ void real_sh_upto(float x, float y, float z, bool unit, float (&Y)[16]) {
+    if (unit) {
+        const float r2 = x * x + y * y + z * z;
+        const float inv = r2 > 0.f ? rsqrtf(r2) : 0.f;
+        x *= inv;
+        y *= inv;
+        z *= inv;
+    }
+    Y[0] = 1.f;
+    if constexpr (L >= 1) {
+        const float s3 = 1.7320508075688772f;
+        Y[1] = s3 * y;
+        Y[2] = s3 * z;
+        Y[3] = s3 * x;
+    }
+    const float x2 = x * x, y2 = y * y, z2 = z * z;
+    if constexpr (L >= 2) {
+        const float s15 = 3.872983346207417f, s5h = 1.118033988749895f;
+        Y[4] = s15 * x * y;
+        Y[5] = s15 * y * z;
+        Y[6] = s5h * (2.f * z2 - x2 - y2);
+        Y[7] = s15 * x * z;
+        Y[8] = 0.5f * s15 * (x2 - y2);
+    }
+    if constexpr (L >= 3) {
+        const float c70 = 2.0916500663351889f;   // sqrt(70)/4
+        const float c105 = 10.246950765959598f;  // sqrt(105)
+        const float c42 = 1.6201851746019651f;   // sqrt(42)/4
+        const float c7 = 1.3228756555322954f;    // sqrt(7)/2
+        Y[9] = c70 * y * (3.f * x2 - y2);
+        Y[10] = c105 * x * y * z;
+        Y[11] = c42 * y * (4.f * z2 - x2 - y2);
+        Y[12] = c7 * z * (2.f * z2 - 3.f * x2 - 3.f * y2);
+        Y[13] = c42 * x * (4.f * z2 - x2 - y2);
+        Y[14] = 0.5f * c105 * z * (x2 - y2);
+        Y[15] = c70 * x * (x2 - 3.f * y2);
     }
 }
 

@@ -89,6 +89,9 @@ struct RingParams {
     int32_t S, eps;                      // stages per warp, edges per chunk (<= 30)
     int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0, source rows, harmonic span
     int32_t m_off, bar_off, warp_bytes;  // warp region: stages, M, barriers
+    int32_t y_off;                       // warp region: harmonics computed from edge vectors [eps][SHN]
+    int32_t vec_mode;                    // 0: `sh` holds harmonic rows; 1/2: `sh` holds edge vectors [E][3],
+                                         // harmonics evaluated here (1: of the unit vector, 2: raw polynomial)
     int32_t tab_bytes;                   // block-shared M recipe table at the start of shared memory
     uint32_t ej[kMaxM];
     float ec[kMaxM][2];
@@ -392,7 +395,9 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     int srcA = load_src(ic), srcB = load_src(lc);
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
-    const int64_t sh_bytes_all = (int64_t)E * SHN * 4;
+    // the streamed per-edge rows: harmonics (SHN floats) or edge vectors (3 floats)
+    const int HR = prm.vec_mode ? 3 : SHN;
+    const int64_t sh_bytes_all = (int64_t)E * HR * 4;
     int n_issued = 0, s_iss = 0;
     auto issue_next = [&]() {
         const int n = ic.n;
@@ -404,9 +409,9 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         const uint32_t okmask = __ballot_sync(0xffffffffu, ok) & (n == 32 ? 0xffffffffu : (1u << n) - 1u);
         // harmonic rows [e, e+n): one bulk copy of the 16-byte aligned span around
         // them; a piece past the array's last 16-byte boundary by plain loads
-        const int64_t b0 = (int64_t)ic.e * SHN * 4, b1 = (int64_t)(ic.e + n) * SHN * 4;
+        const int64_t b0 = (int64_t)ic.e * HR * 4, b1 = (int64_t)(ic.e + n) * HR * 4;
         int64_t a0 = b0, a1 = b1;  // rows of a multiple of 4 floats: the span is aligned already
-        if constexpr (SHN % 4 != 0) {
+        if (HR % 4 != 0) {
             a0 = b0 & ~(int64_t)15;
             a1 = (b1 + 15) & ~(int64_t)15;
             if (a1 > sh_bytes_all) a1 = sh_bytes_all & ~(int64_t)15;
@@ -572,7 +577,20 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             const unsigned char *sb = base + s * prm.stage_bytes;
             // M of the chunk's edges (lane-parallel over entries)
             {
-                const unsigned char *shq = sb + prm.sh_off + (SHN % 4 != 0 ? (e * SHN & 3) * 4 : 0);
+                const unsigned char *shq = sb + prm.sh_off + (HR % 4 != 0 ? (e * HR & 3) * 4 : 0);
+                if (prm.vec_mode) {
+                    // harmonics of the chunk's edge vectors, one edge per lane
+                    float *Y = reinterpret_cast<float *>(base + prm.y_off);
+                    if (lane < n) {
+                        const float *v = reinterpret_cast<const float *>(shq) + 3 * lane;
+                        float yv[16];
+                        real_sh_upto<LSH>(v[0], v[1], v[2], prm.vec_mode == 1, yv);
+#pragma unroll
+                        for (int j = 0; j < SHN; ++j) Y[lane * SHN + j] = yv[j];
+                    }
+                    __syncwarp();
+                    shq = reinterpret_cast<const unsigned char *>(Y);
+                }
                 int4 t[KR];
 #pragma unroll
                 for (int k = 0; k < KR; ++k) t[k] = (lane + 32 * k < P.R) ? tab[lane + 32 * k] : make_int4(0, 0, 0, 0);

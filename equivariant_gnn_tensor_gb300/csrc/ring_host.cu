@@ -96,7 +96,8 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
     g.sh_off = g.f_off + eps * f_bytes;
     g.stage_bytes = round_up(g.sh_off + eps * shn * 4 + 32, 128);  // +32: 16-byte aligned harmonic span
     g.m_off = g.S * g.stage_bytes;
-    g.bar_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
+    g.y_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
+    g.bar_off = round_up(g.y_off + eps * shn * 4, 16);
     g.warp_bytes = round_up(g.bar_off + g.S * 8, 128);
     g.tab_bytes = round_up(16 * TP.R, 128);
     std::memcpy(g.ej, TP.ej, sizeof(uint32_t) * TP.R);
@@ -128,7 +129,10 @@ std::mutex g_plan_mu;
 std::map<PlanKey, std::unique_ptr<RingLaunch>> g_plans;  // nullptr: no ring kernel for this key
 }  // namespace
 
+void mma_cache_forget(uint64_t uid);
+
 void launch_cache_forget(uint64_t uid) {
+    mma_cache_forget(uid);
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (auto it = g_plans.begin(); it != g_plans.end();) it = it->first.uid == uid ? g_plans.erase(it) : std::next(it);
 }
@@ -171,10 +175,12 @@ size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int de
 // Launches the ring kernel (+ partial merge). Returns cudaErrorNotSupported
 // when the descriptor or the pointers do not qualify, or the workspace cannot
 // hold the partials (the caller then uses the generic kernel).
-cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
-                          const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
-                          float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
-                          cudaStream_t stream) {
+// vec_mode 0: `sh` holds harmonic rows [E][dim_sh]; 1 / 2: edge vectors [E][3]
+// whose harmonics the kernel evaluates (1: of the unit vector, 2: raw).
+cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, int vec_mode,
+                          const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
+                          int64_t E, float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin,
+                          int *status, cudaStream_t stream) {
     const TuningState ts = tuning_snapshot();
     if (ts.t.disable_split || !ws || E >= (int64_t)1 << 31) return cudaErrorNotSupported;  // 32-bit edge indices inside
     const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
@@ -193,6 +199,7 @@ cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const
     RingParams prm = rl->geo;
     prm.x = x;
     prm.sh = sh;
+    prm.vec_mode = vec_mode;
     prm.w = w;
     prm.src = src;
     prm.row_ptr = row_ptr;

@@ -212,6 +212,23 @@ TPCONV_API tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
                                      int32_t N_dst, int64_t E, float *out, void *workspace,
                                      size_t workspace_bytes, void *stream);
 
+/* tp_conv_forward with the spherical harmonics evaluated inside the kernel
+ * from edge vectors, so the per-edge harmonic rows never pass through device
+ * memory ("cuEquivariance in PyTorch", Trainable message passing: the
+ * convolution is fed sh(edge_vectors); Spherical harmonics and a NumPy
+ * reference: normalize != 0 takes the harmonics of the unit vector, a zero
+ * vector then giving Y_0 = 1 and zeros; normalize == 0 the raw homogeneous
+ * polynomial). vec: device float32 [E][3] in the destination-sorted edge order,
+ * 16-byte aligned; every other argument as for tp_conv_forward. The harmonics
+ * are those of the descriptor's harmonic irreps, which must be blocks 0..L in
+ * order (the layout the compiled kernels use). Needs a workspace of
+ * tp_conv_forward_workspace_size() bytes; TP_ERR_UNSUPPORTED when the
+ * descriptor has no compiled kernel, the workspace is missing or too small. */
+TPCONV_API tp_status tp_conv_forward_vec(const tp_desc *desc, tp_dtype dtype, const void *x, const float *vec,
+                                         int32_t normalize, const void *w, const int32_t *src,
+                                         const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
+                                         float *out, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Backward pass of tp_conv_forward (float32), the exact gradients of
  * <grad_out, out> with respect to x, w and sh ("cuEquivariance in PyTorch",
  * CPU tensor product and backward: gradients with respect to both inputs and
@@ -243,6 +260,8 @@ TPCONV_API tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out
  *                     up and sets TP_DEV_ERR_TIMEOUT (default 1 s); waits that
  *                     let a failed warp's copies land before it exits always
  *                     keep the 1 s limit.
+ *   disable_mma       1: bfloat16 inputs skip the tensor-core kernel
+ *   mma_stages        shared-memory stages of the tensor-core kernel, 3..8
  * tp_set_tuning(NULL) restores every default. TP_ERR_ARG for a field out of range. */
 typedef struct {
     int32_t ring_stage_bytes;
@@ -252,6 +271,8 @@ typedef struct {
     int32_t ring_pack;
     int32_t disable_split;
     int64_t wait_limit_ns;
+    int32_t disable_mma;
+    int32_t mma_stages;
 } tp_tuning;
 TPCONV_API tp_status tp_set_tuning(const tp_tuning *tuning);
 TPCONV_API tp_status tp_get_tuning(tp_tuning *tuning);

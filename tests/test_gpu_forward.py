@@ -7,7 +7,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import deg_tol, BF16_TOL, FP32_TOL, dev_tensor, err, gpu_sorted_inputs, make_problem, oracle_forward, tuning
+from helpers import (BF16_TOL, FP32_TOL, deg_tol, dev_tensor, err, gpu_sorted_inputs, make_problem, oracle_forward,
+                     rounded, tuning)
 from oracle import cref, so3, tp
 from workloads import WORKLOADS, make_features, make_graph
 
@@ -52,12 +53,16 @@ def test_forward_matches_oracle(tpc, irr, workspace):
 @pytest.mark.parametrize("workspace", ["auto", None], ids=["split", "generic"])
 @pytest.mark.parametrize("irr", SHAPES[:3], ids=lambda c: "|".join(c))
 def test_forward_bf16_inputs(tpc, irr, workspace):
+    """bf16 inputs on the CUDA-core kernels: fp32 math on the same rounded
+    inputs, so the fp32 bound holds too (the tensor-core kernel, which rounds
+    the per-edge matrices to bf16, is disabled here; tests/test_gpu_mma.py)."""
     prob = make_problem(*irr, n_src=200, n_dst=190, E=3000, seed=2)
-    out, _, _ = run(tpc, prob, torch.bfloat16, workspace=workspace)
+    with tuning(tpc, disable_mma=1):
+        out, _, _ = run(tpc, prob, torch.bfloat16, workspace=workspace)
     ref = oracle_forward(prob, torch.bfloat16)
     e = err(out, ref)
     assert e <= BF16_TOL
-    assert e <= FP32_TOL   # fp32 math on the same rounded inputs
+    assert e <= FP32_TOL
 
 
 def test_tiny_workload(tpc):
@@ -122,7 +127,8 @@ def test_bipartite_sources(tpc):
 def test_split_kernel_default_geometry(tpc, irr, dtype):
     """The warp-ring kernel in its default launch geometry against the oracle."""
     prob = make_problem(*irr, n_src=400, n_dst=333, E=9000, seed=14)
-    out, _, _ = run(tpc, prob, dtype)
+    with tuning(tpc, disable_mma=1):
+        out, _, _ = run(tpc, prob, dtype)
     assert err(out, oracle_forward(prob, dtype)) <= FP32_TOL
     assert tpc.tp_device_status(reset=True) == 0
 
@@ -151,7 +157,7 @@ def test_ring_geometries(tpc, irr, dtype, geo):
     dst = np.concatenate([np.full(1000, 7), rng.integers(0, n_dst // 2, 5003) * 2, [n_dst - 1]])
     rng.shuffle(dst)
     prob = make_problem(*irr, n_src=300, n_dst=n_dst, E=len(dst), seed=22, dst=dst)
-    with tuning(tpc, **RING_GEOMETRIES[geo]):
+    with tuning(tpc, disable_mma=1, **RING_GEOMETRIES[geo]):
         out, _, _ = run(tpc, prob, dtype)
     ref = oracle_forward(prob, dtype)
     on = out.double().cpu().numpy()
@@ -263,3 +269,35 @@ def test_wait_timeout_is_reported_and_writes_stay_in_bounds(tpc, mode):
     ref = cref.conv_forward(plan, x.astype(np.float64), sh32[sel], w[sel].astype(np.float64), src[sel], lrp,
                             len(rows))
     assert err(again[torch.as_tensor(rows, device="cuda")], ref) <= FP32_TOL
+
+
+@pytest.mark.parametrize("normalize", [True, False], ids=["unit", "raw"])
+@pytest.mark.parametrize("irr,dtype", [(SHAPES[0], torch.float32), (SHAPES[1], torch.float32),
+                                       (SHAPES[2], torch.bfloat16), (SHAPES[3], torch.float32)],
+                         ids=["tiny", "medium", "large-bf16", "lesson"])
+def test_forward_from_edge_vectors(tpc, irr, dtype, normalize):
+    """tp_conv_forward_vec evaluates the harmonics in the kernel: against the
+    oracle's own (Legendre-based, fp64) harmonics of the same float32 vectors,
+    vectors of random length, several chunks per warp and a ragged tail."""
+    prob = make_problem(*irr, n_src=300, n_dst=257, E=5003, seed=60, normalize=normalize)
+    pl = prob["plan"]
+    v32 = rounded(prob["vec"], torch.float32)
+    prob["sh"] = so3.sh_concat([t.l for t in pl.irr_sh], v32, normalize=normalize)
+    desc = tpc.tp_desc_create(*irr)
+    g = gpu_sorted_inputs(tpc, prob, dtype)
+    vec = dev_tensor(prob["vec"])[g["perm"].long()].contiguous()
+    out = tpc.tp_conv_forward_vec(desc, g["x"], vec, g["w"], g["src"], g["row_ptr"], prob["n_dst"],
+                                  normalize=normalize)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+    assert err(out, oracle_forward(prob, dtype)) <= FP32_TOL
+
+
+def test_forward_from_edge_vectors_needs_a_compiled_kernel(tpc):
+    prob = make_problem(*SHAPES[4], n_src=20, n_dst=20, E=100, seed=61)
+    desc = tpc.tp_desc_create(*SHAPES[4])
+    g = gpu_sorted_inputs(tpc, prob)
+    vec = dev_tensor(prob["vec"])
+    with pytest.raises(tpc.TPError) as ei:
+        tpc.tp_conv_forward_vec(desc, g["x"], vec, g["w"], g["src"], g["row_ptr"], prob["n_dst"])
+    assert tpc.STATUS_NAMES[ei.value.status] == "TP_ERR_UNSUPPORTED"

@@ -56,9 +56,11 @@ def test_fullsize_sampled_rows(tpc, name):
     got = out[torch.as_tensor(rows, device=dev)].double().cpu().numpy()
     deg = row_ptr[rows + 1] - row_ptr[rows]
     assert err(got, ref) <= (BF16_TOL if wl.dtype == "bf16" else FP32_TOL)
-    for g, r, d in zip(got, ref, deg):   # every row against its own magnitude, fp32 math on both
+    for g, r, d in zip(got, ref, deg):   # every row against its own magnitude
         if d:
-            assert err(g, r) <= deg_tol(int(d))
+            # bf16 inputs run on the tensor cores, which round the per-edge
+            # matrices to bf16; fp32 inputs keep fp32 math throughout
+            assert err(g, r) <= (BF16_TOL if wl.dtype == "bf16" else deg_tol(int(d)))
         else:
             assert not np.any(g)
 
