@@ -90,8 +90,7 @@ struct RingParams {
     int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0, source rows, harmonic span
     int32_t m_off, bar_off, warp_bytes;  // warp region: stages, M, barriers
     int32_t y_off;                       // warp region: harmonics computed from edge vectors [eps][SHN]
-    int32_t vec_mode;                    // 0: `sh` holds harmonic rows; 1/2: `sh` holds edge vectors [E][3],
-                                         // harmonics evaluated here (1: of the unit vector, 2: raw polynomial)
+    int32_t vec_mode;                    // kernels with VEC: 1 harmonics of the unit vector, 2 raw polynomial
     int32_t tab_bytes;                   // block-shared M recipe table at the start of shared memory
     uint32_t ej[kMaxM];
     float ec[kMaxM][2];
@@ -321,8 +320,9 @@ __device__ __forceinline__ void store_lane(float *p, const typename LaneVec<CPT,
 }
 
 // CPT channels per lane (mul = 32*CPT), PK: packed pairs of channels. The
-// register cap follows from MINB (blocks of 256 threads per SM).
-template <int LI, int LSH, int LO, int CPT, bool PK, int MINB, typename FT>
+// register cap follows from MINB (blocks of 256 threads per SM). VEC: `sh`
+// holds edge vectors [E][3] and the harmonics are evaluated here.
+template <int LI, int LSH, int LO, int CPT, bool PK, int MINB, typename FT, bool VEC>
 __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(const __grid_constant__ RingParams prm) {
     using LV = LaneVec<CPT, PK>;
     using V = typename LV::V;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     // the streamed per-edge rows: harmonics (SHN floats) or edge vectors (3 floats)
-    const int HR = prm.vec_mode ? 3 : SHN;
+    constexpr int HR = VEC ? 3 : SHN;
     const int64_t sh_bytes_all = (int64_t)E * HR * 4;
     int n_issued = 0, s_iss = 0;
     auto issue_next = [&]() {
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         // them; a piece past the array's last 16-byte boundary by plain loads
         const int64_t b0 = (int64_t)ic.e * HR * 4, b1 = (int64_t)(ic.e + n) * HR * 4;
         int64_t a0 = b0, a1 = b1;  // rows of a multiple of 4 floats: the span is aligned already
-        if (HR % 4 != 0) {
+        if constexpr (HR % 4 != 0) {
             a0 = b0 & ~(int64_t)15;
             a1 = (b1 + 15) & ~(int64_t)15;
             if (a1 > sh_bytes_all) a1 = sh_bytes_all & ~(int64_t)15;
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             // M of the chunk's edges (lane-parallel over entries)
             {
                 const unsigned char *shq = sb + prm.sh_off + (HR % 4 != 0 ? (e * HR & 3) * 4 : 0);
-                if (prm.vec_mode) {
+                if constexpr (VEC) {
                     // harmonics of the chunk's edge vectors, one edge per lane
                     float *Y = reinterpret_cast<float *>(base + prm.y_off);
                     if (lane < n) {

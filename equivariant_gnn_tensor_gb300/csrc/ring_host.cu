@@ -16,6 +16,8 @@ namespace tpc {
 
 const void *ring_kernel_f32(int shape, int cpt, int pk);
 const void *ring_kernel_bf16(int shape, int cpt, int pk);
+const void *ring_kernel_vec_f32(int shape, int cpt, int pk);
+const void *ring_kernel_vec_bf16(int shape, int cpt, int pk);
 
 __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_t *__restrict__ carry_dst,
                                    int n_pieces, int dim_out, int n_dst, float *__restrict__ out) {
@@ -47,6 +49,7 @@ static size_t carry_bytes(int pieces, int dim_out) {
 // shared-memory layout, M recipe, warps per block and blocks per SM.
 struct RingLaunch {
     const void *fn = nullptr;
+    const void *fn_vec = nullptr;  // the same kernel taking edge vectors
     RingParams geo{};  // layout fields and M recipe only
     int wpb = 0, smem = 0, occ = 0, rounds = 1;
 };
@@ -78,7 +81,8 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
     for (int t = 0; t < prog.n; ++t)
         if (TP.wofs[t] != t * mul) return false;
     rl.fn = dtype == TP_F32 ? ring_kernel_f32(TP.shape, cpt, pk) : ring_kernel_bf16(TP.shape, cpt, pk);
-    if (!rl.fn) return false;
+    rl.fn_vec = dtype == TP_F32 ? ring_kernel_vec_f32(TP.shape, cpt, pk) : ring_kernel_vec_bf16(TP.shape, cpt, pk);
+    if (!rl.fn || !rl.fn_vec) return false;
     const int esz = dtype == TP_F32 ? 4 : 2;
     RingParams &g = rl.geo;
     std::memset(&g, 0, sizeof(g));
@@ -107,9 +111,15 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
     rl.smem = g.tab_bytes + wpb * g.warp_bytes;
     if (rl.smem > smem_optin) return false;
     rl.wpb = wpb;
-    if (cudaFuncSetAttribute(rl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess) return false;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rl.occ, rl.fn, 32 * wpb, rl.smem) != cudaSuccess || rl.occ < 1)
+    if (cudaFuncSetAttribute(rl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess ||
+        cudaFuncSetAttribute(rl.fn_vec, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess)
         return false;
+    // both variants launch with the geometry of the smaller occupancy
+    int occ_v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rl.occ, rl.fn, 32 * wpb, rl.smem) != cudaSuccess || rl.occ < 1 ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_v, rl.fn_vec, 32 * wpb, rl.smem) != cudaSuccess || occ_v < 1)
+        return false;
+    if (occ_v < rl.occ) rl.occ = occ_v;
     rl.rounds = tu.ring_rounds ? tu.ring_rounds : 1;
     return true;
 }
@@ -216,7 +226,8 @@ cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const
     prm.wait_ns = ts.t.wait_limit_ns > 0 ? (uint64_t)ts.t.wait_limit_ns : kWaitNs;
     const int blocks = (n_warps + rl->wpb - 1) / rl->wpb;
     void *args[] = {&prm};
-    cudaError_t e = cudaLaunchKernel(rl->fn, dim3(blocks), dim3(32 * rl->wpb), args, (size_t)rl->smem, stream);
+    cudaError_t e = cudaLaunchKernel(vec_mode ? rl->fn_vec : rl->fn, dim3(blocks), dim3(32 * rl->wpb), args,
+                                     (size_t)rl->smem, stream);
     if (e != cudaSuccess) return e;
     const int wpb = 8;
     carry_fixup_kernel<<<(n_pieces + wpb - 1) / wpb, 32 * wpb, 0, stream>>>(prm.carry, prm.carry_dst, n_pieces,
