@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="xlarge", choices=["tiny", "medium", "large", "xlarge"])
-    ap.add_argument("--configs", default="medium,large,tiny,xlarge_vec,medium_vec",
+    ap.add_argument("--configs", default="xlarge_vec,xlarge_mlp,medium,medium_vec,medium_mlp,large,tiny",
                     help="other workloads timed into the same line (comma list; empty for none)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -82,6 +82,13 @@ def measured_peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
     return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peaks file)"
+
+
+def measured_sm_mhz() -> float:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p)).get("sm_max_mhz", 2070.0))
+    return 2070.0
 
 
 def source_hash() -> str:
@@ -205,13 +212,14 @@ def describe(wl, n, E):
     return f"{wl.name}: N={n} E={E} {wl.irreps_in} x {wl.irreps_sh} -> {wl.irreps_out} ({wl.dtype})"
 
 
-def algorithmic_bytes(desc, n, E, esz, from_vectors=False):
-    """Compulsory bytes of one forward: w, sh (or the 12-byte edge vectors when
-    the harmonics are evaluated in the kernel), src, one read of x, one write
-    of out, row pointers."""
+def algorithmic_bytes(desc, n, E, esz, from_vectors=False, radial=False):
+    """Compulsory bytes of one forward: w (none when the radial network computes
+    it in the kernel; its parameters instead), sh (or the 12-byte edge vectors
+    when the harmonics are evaluated in the kernel), src, one read of x, one
+    write of out, row pointers."""
     per_edge_h = 12 if from_vectors else desc.dim_sh * 4
-    return (E * desc.weight_numel * esz + E * per_edge_h + E * 4 + n * desc.dim_x * esz
-            + n * desc.dim_out * 4 + (n + 1) * 4)
+    w_bytes = (16 * 2 + 17 * desc.weight_numel) * 4 if radial else E * desc.weight_numel * esz
+    return (w_bytes + E * per_edge_h + E * 4 + n * desc.dim_x * esz + n * desc.dim_out * 4 + (n + 1) * 4)
 
 
 def backward_bytes(desc, n, E):
@@ -253,16 +261,31 @@ def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 10
             "steps": steps, "kernels": "seg_conv_kernel (dw, dsh by destination; dx by source)"}
 
 
+_BUILT = {}
+
+
 class Forward:
     """One workload's inputs on the device and its forward call; with
     `from_vectors` the call is tp_conv_forward_vec (harmonics evaluated in the
     kernel from the 12-byte edge vectors)."""
 
-    def __init__(self, wname, seed, tpc, torch, device, stream, from_vectors=False):
+    def __init__(self, wname, seed, tpc, torch, device, stream, from_vectors=False, radial=False):
         self.tpc, self.torch, self.stream = tpc, torch, stream
-        self.wl, self.desc, self.inp, self.n, self.E, self.host = build_inputs(wname, seed, tpc, torch, device)
+        key = (wname, seed)
+        if key not in _BUILT:   # one set of device inputs per workload, shared by its variants
+            _BUILT.clear()
+            torch.cuda.empty_cache()
+            _BUILT[key] = build_inputs(wname, seed, tpc, torch, device)
+        self.wl, self.desc, inp, self.n, self.E, self.host = _BUILT[key]
+        self.inp = dict(inp)
         self.vec = self.inp.pop("vec")
-        self.from_vectors = from_vectors
+        self.from_vectors = from_vectors or radial
+        self.radial = radial
+        if radial:   # the weights come from the radial network in the kernel: no weight stream
+            from workloads import make_radial_mlp
+            self.mlp = [torch.as_tensor(a).to(device) for a in make_radial_mlp(seed, self.wl.wid, 16,
+                                                                              self.desc.weight_numel)]
+            del self.inp["w"]
         self.esz = 2 if self.wl.dtype == "bf16" else 4
         self.out = torch.empty((self.n, self.desc.dim_out), dtype=torch.float32, device=device)
         fdt = tpc.TP_BF16_IN_F32_OUT if self.wl.dtype == "bf16" else tpc.TP_F32
@@ -270,11 +293,14 @@ class Forward:
         self.ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device) if ws_bytes else None
         # the warp-ring kernel + its partial-row merge, or the generic kernel alone
         self.launches_per_step = 2 if ws_bytes else 1
-        self.abytes = algorithmic_bytes(self.desc, self.n, self.E, self.esz, from_vectors)
+        self.abytes = algorithmic_bytes(self.desc, self.n, self.E, self.esz, self.from_vectors, radial)
 
     def step(self):
         i = self.inp
-        if self.from_vectors:
+        if self.radial:
+            self.tpc.tp_conv_forward_mlp(self.desc, i["x"], self.vec, *self.mlp, i["src"], i["row_ptr"], self.n,
+                                         out=self.out, workspace=self.ws, stream=self.stream)
+        elif self.from_vectors:
             self.tpc.tp_conv_forward_vec(self.desc, i["x"], self.vec, i["w"], i["src"], i["row_ptr"], self.n,
                                          out=self.out, workspace=self.ws, stream=self.stream)
         else:
@@ -317,7 +343,29 @@ class Forward:
                 "peak_source": peak_src}
 
     def describe(self):
-        return describe(self.wl, self.n, self.E) + (", harmonics from edge vectors" if self.from_vectors else "")
+        extra = (", harmonics and weights (radial network Linear(1,16)-SiLU-Linear(16,P*mul)) from edge vectors"
+                 if self.radial else (", harmonics from edge vectors" if self.from_vectors else ""))
+        return describe(self.wl, self.n, self.E) + extra
+
+    def fma_roofline(self, kernel_ms, sm_mhz):
+        """Radial-network mode is bound by FP32 arithmetic: algorithmic FMAs per
+        edge = 16 per weight (the second layer) + 16 (the first) + the
+        contraction's distinct(i,k) + min(2la+1, 2lc+1) per path and channel,
+        against 152 SMs x 128 FP32 lanes x the maximum SM clock."""
+        from oracle import tp
+        wl = self.wl
+        plan = tp.Plan(wl.irreps_in, wl.irreps_sh, wl.irreps_out)
+        contr = 0
+        for P, C in zip(plan.paths, plan.cg):
+            distinct = int(np.count_nonzero(np.any(C != 0, axis=1)))
+            contr += (distinct + min(2 * P.la + 1, 2 * P.lc + 1)) * plan.mul
+        per_edge = 16 * self.desc.weight_numel + 16 + contr
+        fma = per_edge * self.E
+        achieved = fma / (kernel_ms * 1e-3) / 1e12
+        peak = 152 * 128 * sm_mhz * 1e6 / 1e12
+        return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFMA/s", "frac": achieved / peak,
+                "traffic": None, "fma_per_edge": per_edge, "kernel_us": kernel_ms * 1e3,
+                "peak_source": f"derived: 152 SMs x 128 FP32 lanes x {sm_mhz:.0f} MHz (maximum SM clock)"}
 
     def e2e(self, steps):
         """The same forward through the public call with the inputs in pinned
@@ -502,14 +550,18 @@ def bench_ours(args):
             if name == "tiny":
                 cfgs["tiny"] = tiny_latency(tpc, torch, device, stream)
                 continue
-            base = name[:-4] if name.endswith("_vec") else name
-            g = Forward(base, args.seed, tpc, torch, device, stream, from_vectors=name.endswith("_vec"))
+            base, _, mode = name.partition("_")
+            g = Forward(base, args.seed, tpc, torch, device, stream, from_vectors=mode == "vec",
+                        radial=mode == "mlp")
             k = DEFAULT_STEPS[base]
             _, ms_c, clk = g.timed(k, warmup, local)
             cfgs[name] = {"workload": g.describe(), "value": g.E * k / (ms_c / 1e3), "unit": "edges/s",
                           "steps": k, "kernel_us": ms_c / k * 1e3,
                           "roofline": g.roofline(ms_c / k, peak, peak_src, f"fwd:{name}"), "clocks": clk,
                           "gpu_launches": k * g.launches_per_step}
+            if mode == "mlp":   # arithmetic-bound: the FMA roofline, the byte one beside it
+                cfgs[name]["roofline_bytes"] = cfgs[name]["roofline"]
+                cfgs[name]["roofline"] = g.fma_roofline(ms_c / k, measured_sm_mhz())
             del g
             torch.cuda.empty_cache()
         line["configs"] = cfgs

@@ -40,7 +40,7 @@ TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
 EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
            "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
            "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
-           "tp_conv_forward_vec",
+           "tp_conv_forward_vec", "tp_conv_forward_mlp",
            "tp_conv_backward", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
            "tp_abi_version"]
 
@@ -64,6 +64,11 @@ class _Tuning(ctypes.Structure):
                 ("wait_limit_ns", ctypes.c_int64), ("disable_mma", ctypes.c_int32), ("mma_stages", ctypes.c_int32)]
 
 
+class _Mlp(ctypes.Structure):
+    _fields_ = [("w1", ctypes.c_void_p), ("b1", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("b2", ctypes.c_void_p),
+                ("hidden", ctypes.c_int32)]
+
+
 class _Path(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("a", "b", "c", "la", "lb", "lc")]
 
@@ -81,6 +86,8 @@ _sigs = {
     "tp_conv_forward_workspace_size": [_vp, ctypes.c_int, _i32, _i64, ctypes.POINTER(_sz)],
     "tp_conv_forward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _sz, _vp],
     "tp_conv_forward_vec": [_vp, ctypes.c_int, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _sz, _vp],
+    "tp_conv_forward_mlp": [_vp, ctypes.c_int, _vp, _vp, _i32, ctypes.POINTER(_Mlp), _vp, _vp, _i32, _i32, _i64, _vp,
+                            _vp, _sz, _vp],
     "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
     "tp_set_tuning": [ctypes.POINTER(_Tuning)],
@@ -316,6 +323,32 @@ def tp_conv_forward_vec(desc: Descriptor, x, vec, w, src, row_ptr, n_dst: int, n
                                     _dev_ptr(row_ptr, "row_ptr", torch.int32, 1), x.shape[0], n_dst, E,
                                     _dev_ptr(out, "out", torch.float32, 2), ws_ptr, ws_n, _stream(stream)),
            "tp_conv_forward_vec")
+    return out
+
+
+def tp_conv_forward_mlp(desc: Descriptor, x, vec, w1, b1, w2, b2, src, row_ptr, n_dst: int, normalize: bool = True,
+                        out=None, workspace="auto", stream=None):
+    """tp_conv_forward_vec with the weights computed in the kernel by the radial
+    network silu(|v| w1 + b1) @ w2 + b2 (w1, b1 [16]; w2 [16, weight_numel];
+    b2 [weight_numel]; float32)."""
+    torch = _torch()
+    E = src.shape[0]
+    if out is None:
+        out = torch.empty((n_dst, desc.dim_out), dtype=torch.float32, device=x.device)
+    if isinstance(workspace, str):
+        nb = tp_conv_forward_workspace_size(desc, TP_F32, n_dst, E)
+        workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_n = workspace.numel() if workspace is not None else 0
+    f = torch.float32
+    mlp = _Mlp(_dev_ptr(w1, "w1", f, 1).value, _dev_ptr(b1, "b1", f, 1).value, _dev_ptr(w2, "w2", f, 2).value,
+               _dev_ptr(b2, "b2", f, 1).value, int(w1.shape[0]))
+    _check(_lib.tp_conv_forward_mlp(desc.handle, TP_F32 if x.dtype == f else TP_BF16_IN_F32_OUT,
+                                    _dev_ptr(x, "x", None, 2), _dev_ptr(vec, "vec", f, 2), int(bool(normalize)),
+                                    ctypes.byref(mlp), _dev_ptr(src, "src", torch.int32, 1),
+                                    _dev_ptr(row_ptr, "row_ptr", torch.int32, 1), x.shape[0], n_dst, E,
+                                    _dev_ptr(out, "out", f, 2), ws_ptr, ws_n, _stream(stream)),
+           "tp_conv_forward_mlp")
     return out
 
 

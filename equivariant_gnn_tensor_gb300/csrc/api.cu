@@ -26,9 +26,9 @@ cudaError_t mma_forward(const tp_desc *d, tp_dtype dtype, const void *x, const f
                         float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
                         cudaStream_t stream);
 cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, int vec_mode,
-                          const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
-                          int64_t E, float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin,
-                          int *status, cudaStream_t stream);
+                          const tp_radial_mlp *mlp, const void *w, const int32_t *src, const int32_t *row_ptr,
+                          int32_t N_src, int32_t N_dst, int64_t E, float *out, void *ws, size_t ws_bytes, int dev,
+                          int sms, int smem_optin, int *status, cudaStream_t stream);
 
 // ---- process-wide tuning (tp_set_tuning) ----
 static std::mutex g_tune_mu;
@@ -231,7 +231,7 @@ extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const 
                                     static_cast<cudaStream_t>(stream));
         if (e == cudaSuccess) return TP_OK;
         if (e != cudaErrorNotSupported) return TP_ERR_CUDA;
-        e = split_forward(desc, dtype, x, sh, 0, w, src, row_ptr, N_src, N_dst, E, out, workspace,
+        e = split_forward(desc, dtype, x, sh, 0, nullptr, w, src, row_ptr, N_src, N_dst, E, out, workspace,
                                            workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
                                            static_cast<cudaStream_t>(stream));
         if (e == cudaSuccess) return TP_OK;
@@ -284,8 +284,37 @@ extern "C" tp_status tp_conv_forward_vec(const tp_desc *desc, tp_dtype dtype, co
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
-    const cudaError_t e = split_forward(desc, dtype, x, vec, normalize ? 1 : 2, w, src, row_ptr, N_src, N_dst, E, out,
+    const cudaError_t e = split_forward(desc, dtype, x, vec, normalize ? 1 : 2, nullptr, w, src, row_ptr, N_src, N_dst, E, out,
                                        workspace, workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
+                                       static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) return TP_OK;
+    (void)cudaGetLastError();
+    return e == cudaErrorNotSupported ? TP_ERR_UNSUPPORTED : TP_ERR_CUDA;
+}
+
+extern "C" tp_status tp_conv_forward_mlp(const tp_desc *desc, tp_dtype dtype, const void *x, const float *vec,
+                                         int32_t normalize, const tp_radial_mlp *mlp, const int32_t *src,
+                                         const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E, float *out,
+                                         void *workspace, size_t workspace_bytes, void *stream) {
+    if (!desc || !mlp || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
+    if (dtype != TP_F32 || mlp->hidden != 16) return TP_ERR_UNSUPPORTED;
+    if (N_dst == 0) return TP_OK;
+    if (!out || !row_ptr) return TP_ERR_ARG;
+    if (E > 0 && (!x || !vec || !src || !mlp->w1 || !mlp->b1 || !mlp->w2 || !mlp->b2)) return TP_ERR_ARG;
+    if (E > 0 && N_src == 0) return TP_ERR_INDEX;
+    const Tables &T = desc->tab;
+    if ((T.dim_x * 4) & 15) return TP_ERR_ALIGN;
+    if (!aligned16(out) || (E > 0 && (!aligned16(x) || !aligned16(vec) || !aligned4(src) || !aligned4(mlp->w1) ||
+                                      !aligned4(mlp->b1) || !aligned4(mlp->w2) || !aligned4(mlp->b2))))
+        return TP_ERR_ALIGN;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP_ERR_ALIGN;
+    DevInfo dev;
+    tp_status st = dev_info(dev);
+    if (st != TP_OK) return st;
+    // w is never read in this mode; the weight-row pointer only has to qualify the alignment check
+    const cudaError_t e = split_forward(desc, dtype, x, vec, normalize ? 1 : 2, mlp, x, src, row_ptr, N_src, N_dst, E,
+                                       out, workspace, workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
                                        static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) return TP_OK;
     (void)cudaGetLastError();

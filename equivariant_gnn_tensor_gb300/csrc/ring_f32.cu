@@ -8,12 +8,12 @@ namespace tpc {
 // one channel per lane at 3 blocks per SM and packed pairs at 2.
 const void *ring_kernel_f32(int shape, int cpt, int pk) {
 #define TPC_R(SI, LI, LSH, LO) \
-    if (shape == SI && cpt == 1 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 1, false, 3, float, false>); \
-    if (shape == SI && cpt == 1 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 1, true, 2, float, false>); \
-    if (shape == SI && cpt == 2 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 2, false, 1, float, false>); \
-    if (shape == SI && cpt == 2 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 2, true, 2, float, false>); \
-    if (shape == SI && cpt == 4 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 4, false, 1, float, false>); \
-    if (shape == SI && cpt == 4 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 4, true, 1, float, false>);
+    if (shape == SI && cpt == 1 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 1, false, 3, float, 0>); \
+    if (shape == SI && cpt == 1 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 1, true, 2, float, 0>); \
+    if (shape == SI && cpt == 2 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 2, false, 1, float, 0>); \
+    if (shape == SI && cpt == 2 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 2, true, 2, float, 0>); \
+    if (shape == SI && cpt == 4 && !pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 4, false, 1, float, 0>); \
+    if (shape == SI && cpt == 4 && pk) return reinterpret_cast<const void *>(&ring_fwd_kernel<LI, LSH, LO, 4, true, 1, float, 0>);
     TPC_R(0, 1, 1, 1) TPC_R(1, 1, 2, 2) TPC_R(2, 2, 3, 2) TPC_R(3, 3, 3, 3)
 #undef TPC_R
     return nullptr;

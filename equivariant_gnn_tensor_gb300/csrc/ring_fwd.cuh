@@ -85,12 +85,18 @@ __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_
                                    int dim_out, int n_dst, float *__restrict__ out);
 
 
+// Width of the radial network's hidden layer (Linear(1, 16) -> SiLU -> Linear(16, P*mul)).
+constexpr int kMlpHidden = 16;
+
 struct RingParams {
     int32_t S, eps;                      // stages per warp, edges per chunk (<= 30)
     int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0, source rows, harmonic span
     int32_t m_off, bar_off, warp_bytes;  // warp region: stages, M, barriers
     int32_t y_off;                       // warp region: harmonics computed from edge vectors [eps][SHN]
-    int32_t vec_mode;                    // kernels with VEC: 1 harmonics of the unit vector, 2 raw polynomial
+    int32_t vec_mode;                    // kernels with VM >= 1: 1 harmonics of the unit vector, 2 raw polynomial
+    int32_t h_off;                       // warp region (VM == 2): hidden activations [eps][kMlpHidden]
+    const float *mlp_w1, *mlp_b1;        // VM == 2: [H], [H]
+    const float *mlp_w2, *mlp_b2;        // VM == 2: [H][P*mul] (h-major), [P*mul]
     int32_t tab_bytes;                   // block-shared M recipe table at the start of shared memory
     uint32_t ej[kMaxM];
     float ec[kMaxM][2];
@@ -320,9 +326,12 @@ __device__ __forceinline__ void store_lane(float *p, const typename LaneVec<CPT,
 }
 
 // CPT channels per lane (mul = 32*CPT), PK: packed pairs of channels. The
-// register cap follows from MINB (blocks of 256 threads per SM). VEC: `sh`
-// holds edge vectors [E][3] and the harmonics are evaluated here.
-template <int LI, int LSH, int LO, int CPT, bool PK, int MINB, typename FT, bool VEC>
+// register cap follows from MINB (blocks of 256 threads per SM). VM (vector
+// mode) 0: `sh` holds harmonic rows; 1: `sh` holds edge vectors [E][3] and the
+// harmonics are evaluated here; 2: as 1, and the weight rows are computed here
+// too, by the radial network Linear(1,H) -> SiLU -> Linear(H,P*mul) of the edge
+// length, instead of streamed from `w`.
+template <int LI, int LSH, int LO, int CPT, bool PK, int MINB, typename FT, int VM>
 __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(const __grid_constant__ RingParams prm) {
     using LV = LaneVec<CPT, PK>;
     using V = typename LV::V;
@@ -396,6 +405,8 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_keep = policy_evict_last();
     // the streamed per-edge rows: harmonics (SHN floats) or edge vectors (3 floats)
+    constexpr bool VEC = VM >= 1;
+    static_assert(VM != 2 || sizeof(FT) == 4, "computed weight rows are float32");
     constexpr int HR = VEC ? 3 : SHN;
     const int64_t sh_bytes_all = (int64_t)E * HR * 4;
     int n_issued = 0, s_iss = 0;
@@ -431,7 +442,8 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                     for (int o = lane * 16; o < FB; o += 512)
                         *reinterpret_cast<uint4 *>(sb + prm.f_off + q * FB + o) = make_uint4(0, 0, 0, 0);
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)n * WB + (uint32_t)__popc(okmask) * FB + sh_tma);
+        const uint32_t w_tma = VM == 2 ? 0u : (uint32_t)n * WB;  // VM 2: weight rows computed, not copied
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], w_tma + (uint32_t)__popc(okmask) * FB + sh_tma);
         __syncwarp();
         // one copy per lane: lane 0 the weight rows, lane 1 the harmonic span,
         // lane 2 + q the source row of edge q
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         const int q = lane - 2;
         const void *gsrc = wb + (int64_t)ic.e * WB;
         unsigned char *sdst = sb;
-        uint32_t nbytes = (uint32_t)n * WB;
+        uint32_t nbytes = w_tma;
         uint64_t pol = pol_stream;
         if (lane == 1) {
             gsrc = shb_g + a0;
@@ -575,6 +587,42 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             }
             const int n = min(eps, e_hi - e);
             const unsigned char *sb = base + s * prm.stage_bytes;
+            if constexpr (VM == 2) {
+                // weight rows of the chunk from the radial network of the edge length:
+                // h[q][i] = silu(w1[i] |v_q| + b1[i]), w[q][j] = b2[j] + sum_i w2[i][j] h[q][i]
+                const float *vq = reinterpret_cast<const float *>(sb + prm.sh_off + (e * HR & 3) * 4);
+                float *hq = reinterpret_cast<float *>(base + prm.h_off);
+                constexpr int H = kMlpHidden;
+                for (int t = lane; t < n * H; t += 32) {
+                    const int q = t / H, i = t - q * H;
+                    const float vx = vq[3 * q], vy = vq[3 * q + 1], vz = vq[3 * q + 2];
+                    const float r = sqrtf(vx * vx + vy * vy + vz * vz);
+                    const float z = fmaf(__ldg(prm.mlp_w1 + i), r, __ldg(prm.mlp_b1 + i));
+                    hq[q * H + i] = z / (1.f + expf(-z));
+                }
+                __syncwarp();
+                float *wrows = reinterpret_cast<float *>(const_cast<unsigned char *>(sb));
+                for (int j = lane; j < WNUM; j += 32) {
+                    float w2c[H];
+#pragma unroll
+                    for (int i = 0; i < H; ++i) w2c[i] = __ldg(prm.mlp_w2 + i * WNUM + j);
+                    const float bj = __ldg(prm.mlp_b2 + j);
+                    for (int q = 0; q < n; ++q) {
+                        const float4 *h4 = reinterpret_cast<const float4 *>(hq + q * H);
+                        float a = bj;
+#pragma unroll
+                        for (int i4 = 0; i4 < H / 4; ++i4) {
+                            const float4 hv = h4[i4];
+                            a = fmaf(w2c[4 * i4], hv.x, a);
+                            a = fmaf(w2c[4 * i4 + 1], hv.y, a);
+                            a = fmaf(w2c[4 * i4 + 2], hv.z, a);
+                            a = fmaf(w2c[4 * i4 + 3], hv.w, a);
+                        }
+                        wrows[q * WNUM + j] = a;
+                    }
+                }
+                __syncwarp();
+            }
             // M of the chunk's edges (lane-parallel over entries)
             {
                 const unsigned char *shq = sb + prm.sh_off + (HR % 4 != 0 ? (e * HR & 3) * 4 : 0);

@@ -18,6 +18,7 @@ const void *ring_kernel_f32(int shape, int cpt, int pk);
 const void *ring_kernel_bf16(int shape, int cpt, int pk);
 const void *ring_kernel_vec_f32(int shape, int cpt, int pk);
 const void *ring_kernel_vec_bf16(int shape, int cpt, int pk);
+const void *ring_kernel_mlp_f32(int shape, int cpt, int pk);
 
 __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_t *__restrict__ carry_dst,
                                    int n_pieces, int dim_out, int n_dst, float *__restrict__ out) {
@@ -50,6 +51,7 @@ static size_t carry_bytes(int pieces, int dim_out) {
 struct RingLaunch {
     const void *fn = nullptr;
     const void *fn_vec = nullptr;  // the same kernel taking edge vectors
+    const void *fn_mlp = nullptr;  // ... and computing the weight rows (float32 only; else null)
     RingParams geo{};  // layout fields and M recipe only
     int wpb = 0, smem = 0, occ = 0, rounds = 1;
 };
@@ -82,6 +84,7 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
         if (TP.wofs[t] != t * mul) return false;
     rl.fn = dtype == TP_F32 ? ring_kernel_f32(TP.shape, cpt, pk) : ring_kernel_bf16(TP.shape, cpt, pk);
     rl.fn_vec = dtype == TP_F32 ? ring_kernel_vec_f32(TP.shape, cpt, pk) : ring_kernel_vec_bf16(TP.shape, cpt, pk);
+    rl.fn_mlp = dtype == TP_F32 ? ring_kernel_mlp_f32(TP.shape, cpt, pk) : nullptr;
     if (!rl.fn || !rl.fn_vec) return false;
     const int esz = dtype == TP_F32 ? 4 : 2;
     RingParams &g = rl.geo;
@@ -101,7 +104,8 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
     g.stage_bytes = round_up(g.sh_off + eps * shn * 4 + 32, 128);  // +32: 16-byte aligned harmonic span
     g.m_off = g.S * g.stage_bytes;
     g.y_off = round_up(g.m_off + eps * TP.R * (pk ? 8 : 4), 16);
-    g.bar_off = round_up(g.y_off + eps * shn * 4, 16);
+    g.h_off = round_up(g.y_off + eps * shn * 4, 16);
+    g.bar_off = round_up(g.h_off + eps * kMlpHidden * 4, 16);
     g.warp_bytes = round_up(g.bar_off + g.S * 8, 128);
     g.tab_bytes = round_up(16 * TP.R, 128);
     std::memcpy(g.ej, TP.ej, sizeof(uint32_t) * TP.R);
@@ -120,6 +124,15 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_v, rl.fn_vec, 32 * wpb, rl.smem) != cudaSuccess || occ_v < 1)
         return false;
     if (occ_v < rl.occ) rl.occ = occ_v;
+    if (rl.fn_mlp) {
+        int occ_m = 0;
+        if (cudaFuncSetAttribute(rl.fn_mlp, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_m, rl.fn_mlp, 32 * wpb, rl.smem) != cudaSuccess ||
+            occ_m < 1)
+            rl.fn_mlp = nullptr;
+        else if (occ_m < rl.occ)
+            rl.occ = occ_m;
+    }
     rl.rounds = tu.ring_rounds ? tu.ring_rounds : 1;
     return true;
 }
@@ -186,11 +199,12 @@ size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int de
 // when the descriptor or the pointers do not qualify, or the workspace cannot
 // hold the partials (the caller then uses the generic kernel).
 // vec_mode 0: `sh` holds harmonic rows [E][dim_sh]; 1 / 2: edge vectors [E][3]
-// whose harmonics the kernel evaluates (1: of the unit vector, 2: raw).
+// whose harmonics the kernel evaluates (1: of the unit vector, 2: raw). With
+// `mlp` the weight rows come from the radial network of the edge length (w unused).
 cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, int vec_mode,
-                          const void *w, const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
-                          int64_t E, float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin,
-                          int *status, cudaStream_t stream) {
+                          const tp_radial_mlp *mlp, const void *w, const int32_t *src, const int32_t *row_ptr,
+                          int32_t N_src, int32_t N_dst, int64_t E, float *out, void *ws, size_t ws_bytes, int dev,
+                          int sms, int smem_optin, int *status, cudaStream_t stream) {
     const TuningState ts = tuning_snapshot();
     if (ts.t.disable_split || !ws || E >= (int64_t)1 << 31) return cudaErrorNotSupported;  // 32-bit edge indices inside
     const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
@@ -210,6 +224,13 @@ cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const
     prm.x = x;
     prm.sh = sh;
     prm.vec_mode = vec_mode;
+    if (mlp) {
+        if (!rl->fn_mlp || vec_mode == 0) return cudaErrorNotSupported;
+        prm.mlp_w1 = mlp->w1;
+        prm.mlp_b1 = mlp->b1;
+        prm.mlp_w2 = mlp->w2;
+        prm.mlp_b2 = mlp->b2;
+    }
     prm.w = w;
     prm.src = src;
     prm.row_ptr = row_ptr;
@@ -226,8 +247,8 @@ cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const
     prm.wait_ns = ts.t.wait_limit_ns > 0 ? (uint64_t)ts.t.wait_limit_ns : kWaitNs;
     const int blocks = (n_warps + rl->wpb - 1) / rl->wpb;
     void *args[] = {&prm};
-    cudaError_t e = cudaLaunchKernel(vec_mode ? rl->fn_vec : rl->fn, dim3(blocks), dim3(32 * rl->wpb), args,
-                                     (size_t)rl->smem, stream);
+    const void *fn = mlp ? rl->fn_mlp : (vec_mode ? rl->fn_vec : rl->fn);
+    cudaError_t e = cudaLaunchKernel(fn, dim3(blocks), dim3(32 * rl->wpb), args, (size_t)rl->smem, stream);
     if (e != cudaSuccess) return e;
     const int wpb = 8;
     carry_fixup_kernel<<<(n_pieces + wpb - 1) / wpb, 32 * wpb, 0, stream>>>(prm.carry, prm.carry_dst, n_pieces,

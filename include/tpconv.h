@@ -229,6 +229,32 @@ TPCONV_API tp_status tp_conv_forward_vec(const tp_desc *desc, tp_dtype dtype, co
                                          const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
                                          float *out, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Radial network producing the per-edge weights from the edge length
+ * ("cuEquivariance in PyTorch", Trainable message passing: weights =
+ * radial(|edge_vector|) with radial = Linear(1, 16) -> SiLU -> Linear(16,
+ * weight_numel)):
+ *   h[i] = silu(w1[i] * |v| + b1[i]),  silu(z) = z / (1 + exp(-z)),  i < hidden
+ *   w[j] = b2[j] + sum_i w2[i * weight_numel + j] * h[i],             j < weight_numel
+ * All pointers are device float32: w1[hidden], b1[hidden], w2[hidden][weight_numel]
+ * (hidden-major, i.e. the transpose of a torch Linear(hidden, weight_numel)
+ * weight), b2[weight_numel]. hidden must be 16. */
+typedef struct {
+    const float *w1, *b1;
+    const float *w2, *b2;
+    int32_t hidden;
+} tp_radial_mlp;
+
+/* tp_conv_forward_vec with the per-edge weights computed inside the kernel by
+ * the radial network from the edge length, so the weight stream (the dominant
+ * bytes of the plain forward) is never read from or written to device memory.
+ * float32 only (dtype must be TP_F32); every other argument as for
+ * tp_conv_forward_vec. TP_ERR_UNSUPPORTED for other dtypes, mlp->hidden != 16,
+ * or a descriptor without a compiled kernel / too small a workspace. */
+TPCONV_API tp_status tp_conv_forward_mlp(const tp_desc *desc, tp_dtype dtype, const void *x, const float *vec,
+                                         int32_t normalize, const tp_radial_mlp *mlp, const int32_t *src,
+                                         const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
+                                         float *out, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Backward pass of tp_conv_forward (float32), the exact gradients of
  * <grad_out, out> with respect to x, w and sh ("cuEquivariance in PyTorch",
  * CPU tensor product and backward: gradients with respect to both inputs and

@@ -23,6 +23,9 @@ SegmentedPolynomial: gather and scatter)::
   zero").
 * Features use the ``ir_mul`` layout: block element (i, u) at off + i*mul + u.
 
+Radial network (same page, Trainable message passing): w = radial(|edge vector|)
+with radial = Linear(1, H) -> SiLU -> Linear(H, weight_numel) (``radial_mlp``).
+
 Backward (the map is linear in each of x, sh, w, so these are exact)::
 
     dx[s,a,i,u] = sum_{e: src[e]=s} sum_{p: a_p=a} w[e,p,u] sum_{j,k} C_p[i,j,k] sh[e,b,j] g[dst[e],c,k,u]
@@ -199,6 +202,25 @@ def conv_backward(plan: Plan, x, sh, w, src, dst, g):
     dx = np.zeros_like(x)
     np.add.at(dx, np.asarray(src, dtype=np.int64), dxs)
     return dx, dw, dsh
+
+
+def silu(z):
+    """SiLU (sigmoid-weighted linear unit) z * sigmoid(z) with sigmoid(z) =
+    1 / (1 + exp(-z)), evaluated as exp(-|z|) / (1 + exp(-|z|)) for z < 0 so
+    that no exponential overflows."""
+    z = np.asarray(z, dtype=np.float64)
+    e = np.exp(-np.abs(z))
+    return np.where(z >= 0, z / (1.0 + e), z * e / (1.0 + e))
+
+
+def radial_mlp(vec, w1, b1, w2, b2):
+    """Per-edge weights from the edge length by the radial network of
+    "cuEquivariance in PyTorch", Trainable message passing: Linear(1, H) ->
+    SiLU -> Linear(H, weight_numel) applied to |edge_vector|.
+    vec [E, 3]; w1, b1 [H]; w2 [H, weight_numel]; b2 [weight_numel] -> [E, weight_numel]."""
+    r = np.linalg.norm(np.asarray(vec, dtype=np.float64), axis=1)
+    h = silu(r[:, None] * np.asarray(w1, np.float64)[None, :] + np.asarray(b1, np.float64)[None, :])
+    return h @ np.asarray(w2, np.float64) + np.asarray(b2, np.float64)[None, :]
 
 
 def csr_build(keys, n: int):

@@ -301,3 +301,28 @@ def test_forward_from_edge_vectors_needs_a_compiled_kernel(tpc):
     with pytest.raises(tpc.TPError) as ei:
         tpc.tp_conv_forward_vec(desc, g["x"], vec, g["w"], g["src"], g["row_ptr"], prob["n_dst"])
     assert tpc.STATUS_NAMES[ei.value.status] == "TP_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("irr", [SHAPES[0], SHAPES[1], SHAPES[2], SHAPES[3]], ids=["tiny", "medium", "large", "lesson"])
+def test_forward_with_radial_network(tpc, irr):
+    """tp_conv_forward_mlp computes the weights in the kernel from the edge
+    length (Linear(1,16) -> SiLU -> Linear(16, P*mul)) and the harmonics from
+    the vectors: against the oracle's radial network and harmonics (fp64) of
+    the same float32 inputs."""
+    from workloads import make_radial_mlp
+    prob = make_problem(*irr, n_src=300, n_dst=257, E=4001, seed=62)
+    pl = prob["plan"]
+    w1, b1, w2, b2 = make_radial_mlp(62, 0, 16, pl.weight_numel)
+    v32 = rounded(prob["vec"], torch.float32)
+    prob["w"] = tp.radial_mlp(v32, w1, b1, w2, b2)
+    prob["sh"] = so3.sh_concat([t.l for t in pl.irr_sh], v32)
+    desc = tpc.tp_desc_create(*irr)
+    g = gpu_sorted_inputs(tpc, prob)
+    vec = dev_tensor(prob["vec"])[g["perm"].long()].contiguous()
+    out = tpc.tp_conv_forward_mlp(desc, g["x"], vec, dev_tensor(w1), dev_tensor(b1), dev_tensor(w2), dev_tensor(b2),
+                                  g["src"], g["row_ptr"], prob["n_dst"])
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+    ref = tp.conv_forward(pl, rounded(prob["x"], torch.float32), prob["sh"], prob["w"], prob["src"], prob["dst"],
+                          prob["n_dst"])
+    assert err(out, ref) <= FP32_TOL

@@ -274,3 +274,41 @@ def test_rms_rel_err_hand_computed():
     # an all-zero reference: the plain max difference; an empty tensor: 0
     assert tp.rms_rel_err(np.array([0.0, -0.5]), np.zeros(2)) == 0.5
     assert tp.rms_rel_err(np.zeros((0, 4)), np.zeros((0, 4))) == 0.0
+
+
+def test_silu_identities_and_library():
+    """silu(0) = 0; silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z) = 1);
+    silu(z)/z -> 1 and silu(-z) -> 0 for large z; equal to torch's SiLU in fp64."""
+    import torch
+    z = np.linspace(-30.0, 30.0, 601)
+    s = tp.silu(z)
+    assert tp.silu(0.0) == 0.0
+    np.testing.assert_allclose(s - tp.silu(-z), z, rtol=0, atol=1e-13)
+    assert abs(tp.silu(40.0) / 40.0 - 1.0) < 1e-15 and abs(tp.silu(-40.0)) < 1e-15
+    ref = torch.nn.functional.silu(torch.as_tensor(z, dtype=torch.float64)).numpy()
+    np.testing.assert_allclose(s, ref, rtol=1e-14, atol=1e-300)
+
+
+def test_radial_mlp_structure():
+    """The network's pieces fixed independently of its formula: with w2 = 0 the
+    weights are b2; with w2 the unit matrix e_i (x) e_j, weight j is the hidden
+    unit i = silu(w1_i |v| + b1_i), which depends on the vector only through its
+    length; and the output is affine in (w2, b2)."""
+    rng = np.random.default_rng(5)
+    H, numel, E = 16, 12, 9
+    vec = rng.standard_normal((E, 3))
+    w1, b1 = rng.standard_normal(H), rng.standard_normal(H)
+    b2 = rng.standard_normal(numel)
+    np.testing.assert_array_equal(tp.radial_mlp(vec, w1, b1, np.zeros((H, numel)), b2), np.broadcast_to(b2, (E, numel)))
+    w2 = np.zeros((H, numel))
+    w2[3, 7] = 1.0
+    out = tp.radial_mlp(vec, w1, b1, w2, np.zeros(numel))
+    r = np.linalg.norm(vec, axis=1)
+    np.testing.assert_allclose(out[:, 7], tp.silu(w1[3] * r + b1[3]), rtol=1e-15)
+    assert not np.any(np.delete(out, 7, axis=1))
+    R = so3.random_rotation(rng)   # rotating (or flipping) the vectors changes nothing
+    np.testing.assert_allclose(tp.radial_mlp(-vec @ R.T, w1, b1, w2, b2), tp.radial_mlp(vec, w1, b1, w2, b2), rtol=1e-13)
+    wa, wb = rng.standard_normal((H, numel)), rng.standard_normal((H, numel))
+    ba, bb = rng.standard_normal(numel), rng.standard_normal(numel)
+    np.testing.assert_allclose(tp.radial_mlp(vec, w1, b1, wa + wb, ba + bb),
+                               tp.radial_mlp(vec, w1, b1, wa, ba) + tp.radial_mlp(vec, w1, b1, wb, bb), rtol=1e-12)

@@ -29,7 +29,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "radius_graph", "make_graph", "make_features"]
+__all__ = ["Workload", "WORKLOADS", "radius_graph", "make_graph", "make_features", "make_radial_mlp"]
 
 
 @dataclass(frozen=True)
@@ -188,6 +188,19 @@ def make_features(rng: np.random.Generator, w: Workload, n_nodes: int, n_edges: 
         wt *= dtype(1.0 / math.sqrt(n_paths))
     g = rng.standard_normal((n_nodes, dim_out), dtype=dtype) if w.backward else None
     return x, wt, g
+
+
+def make_radial_mlp(seed: int, wid: int, hidden: int, weight_numel: int, dtype=np.float32):
+    """Parameters of a radial network Linear(1, hidden) -> SiLU ->
+    Linear(hidden, weight_numel): w1, b1 ~ N(0, 1) [hidden]; w2 ~ N(0, 1/hidden)
+    [hidden, weight_numel] (hidden-major); b2 ~ N(0, 0.01) [weight_numel]. Drawn
+    from a stream of their own, default_rng([seed, wid, 7])."""
+    rng = np.random.default_rng([seed, wid, 7])
+    w1 = rng.standard_normal(hidden).astype(dtype)
+    b1 = rng.standard_normal(hidden).astype(dtype)
+    w2 = (rng.standard_normal((hidden, weight_numel)) / math.sqrt(hidden)).astype(dtype)
+    b2 = (0.1 * rng.standard_normal(weight_numel)).astype(dtype)
+    return w1, b1, w2, b2
 
 
 def subgraph_uniform(seed: int, n_nodes: int, n_edges: int, wid: int = 99):
