@@ -37,10 +37,12 @@ STATUS_NAMES = {0: "TP_OK", 1: "TP_ERR_PARSE", 2: "TP_ERR_UNSUPPORTED", 4: "TP_E
 TP_F32, TP_BF16_IN_F32_OUT = 0, 1
 TP_IR_MUL, TP_MUL_IR = 0, 1
 TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
+TP_REDUCE_SUM, TP_REDUCE_MEAN = 0, 1
 EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
            "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
            "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
-           "tp_conv_forward_vec", "tp_conv_forward_mlp",
+           "tp_conv_forward_vec", "tp_conv_forward_mlp", "tp_conv_forward_ex_workspace_size", "tp_conv_forward_ex",
+           "tp_transpose_layout",
            "tp_conv_backward", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
            "tp_abi_version"]
 
@@ -55,7 +57,7 @@ class TPError(RuntimeError):
 class _Info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_paths", "mul", "dim_x", "dim_sh", "dim_out", "weight_numel", "n_in", "n_sh", "n_out",
-        "lmax_in", "lmax_sh", "lmax_out", "cg_nnz")]
+        "lmax_in", "lmax_sh", "lmax_out", "cg_nnz", "layout")]
 
 
 class _Tuning(ctypes.Structure):
@@ -67,6 +69,15 @@ class _Tuning(ctypes.Structure):
 class _Mlp(ctypes.Structure):
     _fields_ = [("w1", ctypes.c_void_p), ("b1", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("b2", ctypes.c_void_p),
                 ("hidden", ctypes.c_int32)]
+
+
+class _FwdArgs(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("x", ctypes.c_void_p), ("sh", ctypes.c_void_p), ("vec", ctypes.c_void_p),
+                ("normalize", ctypes.c_int32), ("mlp", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("src", ctypes.c_void_p), ("row_ptr", ctypes.c_void_p), ("index_bits", ctypes.c_int32),
+                ("reduce", ctypes.c_int32), ("N_src", ctypes.c_int32), ("N_dst", ctypes.c_int32),
+                ("E", ctypes.c_int64), ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class _Path(ctypes.Structure):
@@ -88,6 +99,9 @@ _sigs = {
     "tp_conv_forward_vec": [_vp, ctypes.c_int, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _sz, _vp],
     "tp_conv_forward_mlp": [_vp, ctypes.c_int, _vp, _vp, _i32, ctypes.POINTER(_Mlp), _vp, _vp, _i32, _i32, _i64, _vp,
                             _vp, _sz, _vp],
+    "tp_conv_forward_ex_workspace_size": [_vp, ctypes.POINTER(_FwdArgs), ctypes.POINTER(_sz)],
+    "tp_conv_forward_ex": [_vp, ctypes.POINTER(_FwdArgs), _vp],
+    "tp_transpose_layout": [_vp, _i32, ctypes.c_int, _vp, _vp, _i64, _i32, _vp],
     "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
     "tp_set_tuning": [ctypes.POINTER(_Tuning)],
@@ -350,6 +364,57 @@ def tp_conv_forward_mlp(desc: Descriptor, x, vec, w1, b1, w2, b2, src, row_ptr, 
                                     _dev_ptr(out, "out", f, 2), ws_ptr, ws_n, _stream(stream)),
            "tp_conv_forward_mlp")
     return out
+
+
+def tp_conv_forward_ex(desc: Descriptor, x, src, row_ptr, n_dst: int, w=None, sh=None, vec=None, normalize=True,
+                       mlp=None, reduce: str = "sum", out=None, workspace=None, stream=None):
+    """The forward with int32 or int64 indices (src, row_ptr dtype), the
+    descriptor's layout for x and out (mul_ir converted on the device), and
+    reduce "sum" or "mean". Harmonics as rows `sh` or from edge vectors `vec`;
+    mlp = (w1, b1, w2, b2) computes the weights from the edge length (needs vec)."""
+    torch = _torch()
+    E = src.shape[0]
+    if src.dtype != row_ptr.dtype or src.dtype not in (torch.int32, torch.int64):
+        raise TypeError("src and row_ptr must both be int32 or both int64")
+    f = torch.float32
+    dtype = TP_F32 if x.dtype == f else TP_BF16_IN_F32_OUT
+    if out is None:
+        out = torch.empty((n_dst, desc.dim_out), dtype=f, device=x.device)
+    keep = []
+    mlp_p = None
+    if mlp is not None:
+        w1, b1, w2, b2 = mlp
+        m = _Mlp(_dev_ptr(w1, "w1", f, 1).value, _dev_ptr(b1, "b1", f, 1).value, _dev_ptr(w2, "w2", f, 2).value,
+                 _dev_ptr(b2, "b2", f, 1).value, int(w1.shape[0]))
+        keep.append(m)
+        mlp_p = ctypes.addressof(m)
+    a = _FwdArgs(dtype, _dev_ptr(x, "x", None, 2).value, _dev_ptr(sh, "sh", f, 2).value,
+                 _dev_ptr(vec, "vec", f, 2).value, int(bool(normalize)), mlp_p, _dev_ptr(w, "w", None, 2).value,
+                 _dev_ptr(src, "src", None, 1).value, _dev_ptr(row_ptr, "row_ptr", None, 1).value,
+                 64 if src.dtype == torch.int64 else 32, {"sum": TP_REDUCE_SUM, "mean": TP_REDUCE_MEAN}[reduce],
+                 x.shape[0], n_dst, E, _dev_ptr(out, "out", f, 2).value, None, 0)
+    n = _sz()
+    _check(_lib.tp_conv_forward_ex_workspace_size(desc.handle, ctypes.byref(a), ctypes.byref(n)),
+           "tp_conv_forward_ex_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(max(int(n.value), 1), dtype=torch.uint8, device=x.device)
+    a.workspace = _dev_ptr(workspace, "workspace", torch.uint8).value
+    a.workspace_bytes = workspace.numel()
+    _check(_lib.tp_conv_forward_ex(desc.handle, ctypes.byref(a), _stream(stream)), "tp_conv_forward_ex")
+    return out
+
+
+def tp_transpose_layout(desc: Descriptor, which: str, source: str, src, dst=None, stream=None):
+    """Blockwise mul_ir <-> ir_mul conversion of rows of the desc's input
+    (which="in") or output (which="out") irreps; `source` is src's layout."""
+    torch = _torch()
+    if dst is None:
+        dst = torch.empty_like(src)
+    lay = {"ir_mul": TP_IR_MUL, "mul_ir": TP_MUL_IR}[source]
+    _check(_lib.tp_transpose_layout(desc.handle, {"in": 0, "out": 1}[which], lay, _dev_ptr(src, "src", None, 2),
+                                    _dev_ptr(dst, "dst", None, 2), src.shape[0], src.element_size(), _stream(stream)),
+           "tp_transpose_layout")
+    return dst
 
 
 def tp_conv_backward(desc: Descriptor, grad_out, x, sh, w, src, dst, row_ptr, src_perm, src_row_ptr,

@@ -20,6 +20,11 @@ cudaError_t sh_launch(const float *vec, int64_t E, int normalize, const Tables &
 int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
 size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
+cudaError_t indices_to_i32(const int64_t *in, int64_t n, int32_t *out, cudaStream_t stream);
+cudaError_t transpose_rows(const tp_desc *d, int which, int from, const void *src, void *dst, int64_t rows,
+                           int elem_bytes, cudaStream_t stream);
+cudaError_t scale_rows_by_inverse_degree(float *out, const int32_t *row_ptr, int32_t n, int32_t dim,
+                                         cudaStream_t stream);
 size_t mma_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
 cudaError_t mma_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
                         const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
@@ -205,120 +210,228 @@ extern "C" tp_status tp_conv_forward_workspace_size(const tp_desc *desc, tp_dtyp
     return TP_OK;
 }
 
-extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const void *x, const float *sh, const void *w,
-                                     const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
-                                     int64_t E, float *out, void *workspace, size_t workspace_bytes, void *stream) {
-    if (!desc || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
-    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
-    if (N_dst == 0) return TP_OK;
-    if (!out || !row_ptr) return TP_ERR_ARG;
-    if (E > 0 && (!x || !sh || !w || !src)) return TP_ERR_ARG;
-    if (E > 0 && N_src == 0) return TP_ERR_INDEX;
+namespace {
+
+// Arguments of one forward, after the entry point's own conversions.
+struct FwdArgs {
+    tp_dtype dtype;
+    const void *x;
+    const float *sh;  // harmonic rows, or edge vectors when vec_mode != 0
+    int vec_mode;     // 0 rows; 1 / 2 vectors (unit / raw harmonics)
+    const tp_radial_mlp *mlp;
+    const void *w;
+    const int32_t *src, *row_ptr;
+    int32_t N_src, N_dst;
+    int64_t E;
+    float *out;
+    void *ws;
+    size_t ws_bytes;
+};
+
+// Checks and dispatch shared by every forward entry point: the tensor-core
+// kernel (bfloat16 harmonic rows), the warp-ring kernel, then the generic one
+// (harmonic rows only).
+tp_status forward_core(const tp_desc *desc, const FwdArgs &a, cudaStream_t stream) {
+    if (a.N_src < 0 || a.N_dst < 0 || a.E < 0 || a.E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (a.dtype != TP_F32 && a.dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
+    if (a.mlp && (a.dtype != TP_F32 || a.mlp->hidden != 16 || a.vec_mode == 0)) return TP_ERR_UNSUPPORTED;
+    if (a.N_dst == 0) return TP_OK;
+    if (!a.out || !a.row_ptr) return TP_ERR_ARG;
+    if (a.E > 0 && (!a.x || !a.sh || !a.src || (!a.w && !a.mlp))) return TP_ERR_ARG;
+    if (a.E > 0 && a.mlp && (!a.mlp->w1 || !a.mlp->b1 || !a.mlp->w2 || !a.mlp->b2)) return TP_ERR_ARG;
+    if (a.E > 0 && a.N_src == 0) return TP_ERR_INDEX;
     const Tables &T = desc->tab;
-    const int esz = dtype == TP_F32 ? 4 : 2;
+    const int esz = a.dtype == TP_F32 ? 4 : 2;
     const int f_bytes = T.dim_x * esz, w_bytes = T.wnum * esz;
     if ((f_bytes & 15) || (w_bytes & 15)) return TP_ERR_ALIGN;
-    if (!aligned16(out) || (E > 0 && (!aligned16(x) || !aligned16(w) || !aligned4(sh) || !aligned4(src))))
+    // weight rows are never read with a radial network: x stands in for the alignment check
+    const void *w = a.mlp ? a.x : a.w;
+    if (!aligned16(a.out) || (a.E > 0 && (!aligned16(a.x) || !aligned16(w) || !aligned4(a.src) ||
+                                          (a.vec_mode ? !aligned16(a.sh) : !aligned4(a.sh)))))
         return TP_ERR_ALIGN;
-    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP_ERR_ALIGN;
-    {
-        DevInfo dev;
-        tp_status st = dev_info(dev);
-        if (st != TP_OK) return st;
-        // bfloat16 inputs: the tensor-core kernel first
-        cudaError_t e = mma_forward(desc, dtype, x, sh, w, src, row_ptr, N_src, N_dst, E, out, workspace,
-                                    workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
-                                    static_cast<cudaStream_t>(stream));
-        if (e == cudaSuccess) return TP_OK;
-        if (e != cudaErrorNotSupported) return TP_ERR_CUDA;
-        e = split_forward(desc, dtype, x, sh, 0, nullptr, w, src, row_ptr, N_src, N_dst, E, out, workspace,
-                                           workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
-                                           static_cast<cudaStream_t>(stream));
-        if (e == cudaSuccess) return TP_OK;
-        if (e != cudaErrorNotSupported) return TP_ERR_CUDA;
-        (void)cudaGetLastError();
-    }
-    Shape shp;
-    if (!pick_shape(desc->lmax_in, desc->lmax_out, shp)) return TP_ERR_UNSUPPORTED;
-    const int cpt = pick_cpt(T.mul);
-    const void *fn = dtype == TP_F32 ? seg_fwd_f32_kernel(shp, cpt) : seg_fwd_bf16_kernel(shp, cpt);
-    if (!fn) return TP_ERR_UNSUPPORTED;
+    if (a.mlp && a.E > 0 &&
+        (!aligned4(a.mlp->w1) || !aligned4(a.mlp->b1) || !aligned4(a.mlp->w2) || !aligned4(a.mlp->b2)))
+        return TP_ERR_ALIGN;
+    if (a.ws && (reinterpret_cast<uintptr_t>(a.ws) & 255u)) return TP_ERR_ALIGN;
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
+    cudaError_t e = cudaErrorNotSupported;
+    if (a.vec_mode == 0)  // bfloat16 harmonic rows: the tensor-core kernel first
+        e = mma_forward(desc, a.dtype, a.x, a.sh, w, a.src, a.row_ptr, a.N_src, a.N_dst, a.E, a.out, a.ws, a.ws_bytes,
+                        dev.dev, dev.sms, dev.smem_optin, dev.status, stream);
+    if (e == cudaErrorNotSupported)
+        e = split_forward(desc, a.dtype, a.x, a.sh, a.vec_mode, a.mlp, w, a.src, a.row_ptr, a.N_src, a.N_dst, a.E,
+                          a.out, a.ws, a.ws_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status, stream);
+    if (e == cudaSuccess) return TP_OK;
+    if (e != cudaErrorNotSupported) return TP_ERR_CUDA;
+    (void)cudaGetLastError();
+    if (a.vec_mode != 0) return TP_ERR_UNSUPPORTED;  // edge vectors need a compiled kernel and a workspace
+    Shape shp;
+    if (!pick_shape(desc->lmax_in, desc->lmax_out, shp)) return TP_ERR_UNSUPPORTED;
+    const int cpt = pick_cpt(T.mul);
+    const void *fn = a.dtype == TP_F32 ? seg_fwd_f32_kernel(shp, cpt) : seg_fwd_bf16_kernel(shp, cpt);
+    if (!fn) return TP_ERR_UNSUPPORTED;
     SegParams prm;
     std::memset(&prm, 0, sizeof(prm));
     int warps = 0, grid = 0, smem = 0;
-    st = plan_launch(fn, dev, kTablesBytes, w_bytes, f_bytes, T.dim_sh, T.R, false, N_dst, prm.lay, warps, grid, smem);
+    st = plan_launch(fn, dev, kTablesBytes, w_bytes, f_bytes, T.dim_sh, T.R, false, a.N_dst, prm.lay, warps, grid,
+                     smem);
     if (st != TP_OK) return st;
     prm.tab = T;
-    prm.feat = x;
-    prm.sh = sh;
-    prm.w = w;
-    prm.gidx = src;
-    prm.seg_ptr = row_ptr;
-    prm.out = out;
+    prm.feat = a.x;
+    prm.sh = a.sh;
+    prm.w = a.w;
+    prm.gidx = a.src;
+    prm.seg_ptr = a.row_ptr;
+    prm.out = a.out;
     prm.status = dev.status;
-    prm.n_seg = N_dst;
-    prm.n_gather = N_src;
-    prm.n_edges = E;
-    return launch_seg(fn, prm, grid, warps, smem, static_cast<cudaStream_t>(stream));
+    prm.n_seg = a.N_dst;
+    prm.n_gather = a.N_src;
+    prm.n_edges = a.E;
+    return launch_seg(fn, prm, grid, warps, smem, stream);
+}
+
+}  // namespace
+
+extern "C" tp_status tp_conv_forward(const tp_desc *desc, tp_dtype dtype, const void *x, const float *sh, const void *w,
+                                     const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst,
+                                     int64_t E, float *out, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!desc) return TP_ERR_ARG;
+    if (desc->layout != TP_IR_MUL) return TP_ERR_UNSUPPORTED;
+    const FwdArgs a{dtype, x, sh, 0, nullptr, w, src, row_ptr, N_src, N_dst, E, out, workspace, workspace_bytes};
+    return forward_core(desc, a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" tp_status tp_conv_forward_vec(const tp_desc *desc, tp_dtype dtype, const void *x, const float *vec,
                                          int32_t normalize, const void *w, const int32_t *src, const int32_t *row_ptr,
                                          int32_t N_src, int32_t N_dst, int64_t E, float *out, void *workspace,
                                          size_t workspace_bytes, void *stream) {
-    if (!desc || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
-    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
-    if (N_dst == 0) return TP_OK;
-    if (!out || !row_ptr) return TP_ERR_ARG;
-    if (E > 0 && (!x || !vec || !w || !src)) return TP_ERR_ARG;
-    if (E > 0 && N_src == 0) return TP_ERR_INDEX;
-    const Tables &T = desc->tab;
-    const int esz = dtype == TP_F32 ? 4 : 2;
-    if (((T.dim_x * esz) & 15) || ((T.wnum * esz) & 15)) return TP_ERR_ALIGN;
-    if (!aligned16(out) || (E > 0 && (!aligned16(x) || !aligned16(w) || !aligned16(vec) || !aligned4(src))))
-        return TP_ERR_ALIGN;
-    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP_ERR_ALIGN;
-    DevInfo dev;
-    tp_status st = dev_info(dev);
-    if (st != TP_OK) return st;
-    const cudaError_t e = split_forward(desc, dtype, x, vec, normalize ? 1 : 2, nullptr, w, src, row_ptr, N_src, N_dst, E, out,
-                                       workspace, workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
-                                       static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess) return TP_OK;
-    (void)cudaGetLastError();
-    return e == cudaErrorNotSupported ? TP_ERR_UNSUPPORTED : TP_ERR_CUDA;
+    if (!desc) return TP_ERR_ARG;
+    if (desc->layout != TP_IR_MUL) return TP_ERR_UNSUPPORTED;
+    const FwdArgs a{dtype, x, vec, normalize ? 1 : 2, nullptr, w, src, row_ptr, N_src, N_dst, E, out, workspace,
+                    workspace_bytes};
+    return forward_core(desc, a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" tp_status tp_conv_forward_mlp(const tp_desc *desc, tp_dtype dtype, const void *x, const float *vec,
                                          int32_t normalize, const tp_radial_mlp *mlp, const int32_t *src,
                                          const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E, float *out,
                                          void *workspace, size_t workspace_bytes, void *stream) {
-    if (!desc || !mlp || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
-    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
-    if (dtype != TP_F32 || mlp->hidden != 16) return TP_ERR_UNSUPPORTED;
-    if (N_dst == 0) return TP_OK;
-    if (!out || !row_ptr) return TP_ERR_ARG;
-    if (E > 0 && (!x || !vec || !src || !mlp->w1 || !mlp->b1 || !mlp->w2 || !mlp->b2)) return TP_ERR_ARG;
-    if (E > 0 && N_src == 0) return TP_ERR_INDEX;
-    const Tables &T = desc->tab;
-    if ((T.dim_x * 4) & 15) return TP_ERR_ALIGN;
-    if (!aligned16(out) || (E > 0 && (!aligned16(x) || !aligned16(vec) || !aligned4(src) || !aligned4(mlp->w1) ||
-                                      !aligned4(mlp->b1) || !aligned4(mlp->w2) || !aligned4(mlp->b2))))
-        return TP_ERR_ALIGN;
-    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP_ERR_ALIGN;
+    if (!desc || !mlp) return TP_ERR_ARG;
+    if (desc->layout != TP_IR_MUL) return TP_ERR_UNSUPPORTED;
+    const FwdArgs a{dtype, x, vec, normalize ? 1 : 2, mlp, nullptr, src, row_ptr, N_src, N_dst, E, out, workspace,
+                    workspace_bytes};
+    return forward_core(desc, a, static_cast<cudaStream_t>(stream));
+}
+
+// ---- tp_conv_forward_ex: index width, layout and reduction around the core ----
+
+namespace {
+
+size_t al256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Workspace of tp_conv_forward_ex: the core forward's, then (as needed) int32
+// copies of src and row_ptr, an ir_mul copy of x and an ir_mul out.
+struct ExLayout {
+    size_t core, src32, rp32, x_ir, out_ir, total;
+};
+
+tp_status ex_layout(const tp_desc *desc, const tp_forward_args *a, ExLayout &L) {
+    if (!a || a->N_src < 0 || a->N_dst < 0 || a->E < 0 || a->E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (a->dtype != TP_F32 && a->dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
+    if (a->index_bits != 32 && a->index_bits != 64) return TP_ERR_ARG;
+    if (a->reduce != TP_REDUCE_SUM && a->reduce != TP_REDUCE_MEAN) return TP_ERR_ARG;
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
-    // w is never read in this mode; the weight-row pointer only has to qualify the alignment check
-    const cudaError_t e = split_forward(desc, dtype, x, vec, normalize ? 1 : 2, mlp, x, src, row_ptr, N_src, N_dst, E,
-                                       out, workspace, workspace_bytes, dev.dev, dev.sms, dev.smem_optin, dev.status,
-                                       static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess) return TP_OK;
-    (void)cudaGetLastError();
-    return e == cudaErrorNotSupported ? TP_ERR_UNSUPPORTED : TP_ERR_CUDA;
+    const size_t c1 = split_workspace_bytes(desc, a->dtype, a->E, dev.dev, dev.sms, dev.smem_optin);
+    const size_t c2 = a->vec ? 0 : mma_workspace_bytes(desc, a->dtype, a->E, dev.dev, dev.sms, dev.smem_optin);
+    const Tables &T = desc->tab;
+    const size_t esz = a->dtype == TP_F32 ? 4 : 2;
+    const bool i64 = a->index_bits == 64, mi = desc->layout == TP_MUL_IR;
+    L.core = al256(c1 > c2 ? c1 : c2);
+    L.src32 = L.core;
+    L.rp32 = L.src32 + (i64 ? al256((size_t)a->E * 4) : 0);
+    L.x_ir = L.rp32 + (i64 ? al256(((size_t)a->N_dst + 1) * 4) : 0);
+    L.out_ir = L.x_ir + (mi ? al256((size_t)a->N_src * T.dim_x * esz) : 0);
+    L.total = L.out_ir + (mi ? al256((size_t)a->N_dst * T.dim_out * 4) : 0);
+    return TP_OK;
+}
+
+}  // namespace
+
+extern "C" tp_status tp_conv_forward_ex_workspace_size(const tp_desc *desc, const tp_forward_args *args,
+                                                       size_t *bytes) {
+    if (!desc || !bytes) return TP_ERR_ARG;
+    ExLayout L;
+    const tp_status st = ex_layout(desc, args, L);
+    if (st != TP_OK) return st;
+    *bytes = L.total;
+    return TP_OK;
+}
+
+extern "C" tp_status tp_conv_forward_ex(const tp_desc *desc, const tp_forward_args *a, void *stream) {
+    if (!desc || !a) return TP_ERR_ARG;
+    ExLayout L;
+    tp_status st = ex_layout(desc, a, L);
+    if (st != TP_OK) return st;
+    if (a->N_dst == 0) return TP_OK;
+    if (!a->workspace || a->workspace_bytes < L.total) return TP_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return TP_ERR_ALIGN;
+    if (!a->out || !a->row_ptr || (a->E > 0 && (!a->x || !a->src))) return TP_ERR_ARG;
+    if (a->sh && a->vec) return TP_ERR_ARG;  // harmonic rows or edge vectors, not both
+    if (a->mlp && !a->vec) return TP_ERR_UNSUPPORTED;
+    DevInfo dev;
+    st = dev_info(dev);
+    if (st != TP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(a->workspace);
+    const Tables &T = desc->tab;
+    const int esz = a->dtype == TP_F32 ? 4 : 2;
+    const int32_t *src = static_cast<const int32_t *>(a->src), *rp = static_cast<const int32_t *>(a->row_ptr);
+    if (a->index_bits == 64) {  // int32 copies (out-of-range values become invalid indices the kernels flag)
+        if (indices_to_i32(static_cast<const int64_t *>(a->src), a->E, reinterpret_cast<int32_t *>(ws + L.src32), s) !=
+                cudaSuccess ||
+            indices_to_i32(static_cast<const int64_t *>(a->row_ptr), (int64_t)a->N_dst + 1,
+                           reinterpret_cast<int32_t *>(ws + L.rp32), s) != cudaSuccess)
+            return TP_ERR_CUDA;
+        src = reinterpret_cast<const int32_t *>(ws + L.src32);
+        rp = reinterpret_cast<const int32_t *>(ws + L.rp32);
+    }
+    const void *x = a->x;
+    float *out = a->out;
+    if (desc->layout == TP_MUL_IR) {
+        if (a->N_src > 0 && a->E > 0 &&
+            transpose_rows(desc, 0, TP_MUL_IR, a->x, ws + L.x_ir, a->N_src, esz, s) != cudaSuccess)
+            return TP_ERR_CUDA;
+        x = ws + L.x_ir;
+        out = reinterpret_cast<float *>(ws + L.out_ir);
+    }
+    const FwdArgs f{a->dtype, x, a->vec ? a->vec : a->sh, a->vec ? (a->normalize ? 1 : 2) : 0, a->mlp, a->w, src, rp,
+                    a->N_src, a->N_dst, a->E, out, a->workspace, L.core};
+    st = forward_core(desc, f, s);
+    if (st != TP_OK) return st;
+    if (a->reduce == TP_REDUCE_MEAN && scale_rows_by_inverse_degree(out, rp, a->N_dst, T.dim_out, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    if (desc->layout == TP_MUL_IR && transpose_rows(desc, 1, TP_IR_MUL, out, a->out, a->N_dst, 4, s) != cudaSuccess)
+        return TP_ERR_CUDA;
+    return TP_OK;
+}
+
+extern "C" tp_status tp_transpose_layout(const tp_desc *desc, int32_t which, tp_layout from, const void *src,
+                                         void *dst, int64_t rows, int32_t elem_bytes, void *stream) {
+    if (!desc || (which != 0 && which != 1) || (from != TP_IR_MUL && from != TP_MUL_IR) || rows < 0 ||
+        (elem_bytes != 2 && elem_bytes != 4))
+        return TP_ERR_ARG;
+    if (rows == 0) return TP_OK;
+    if (!src || !dst || src == dst) return TP_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & (uintptr_t)(elem_bytes - 1))
+        return TP_ERR_ALIGN;
+    return transpose_rows(desc, which, from, src, dst, rows, elem_bytes, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? TP_OK
+               : TP_ERR_CUDA;
 }
 
 extern "C" tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out, const float *x, const float *sh,
@@ -326,6 +439,7 @@ extern "C" tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out
                                       const int32_t *src_perm, const int32_t *src_row_ptr, int32_t N_src,
                                       int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh, void *stream) {
     if (!desc || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (desc->layout != TP_IR_MUL) return TP_ERR_UNSUPPORTED;
     if ((N_src > 0 && (!dx || !src_row_ptr)) || (N_dst > 0 && !row_ptr)) return TP_ERR_ARG;
     if (E > 0 && (!grad_out || !x || !sh || !w || !src || !dst || !src_perm || !dw || !dsh)) return TP_ERR_ARG;
     if (E > 0 && (N_src == 0 || N_dst == 0)) return TP_ERR_INDEX;

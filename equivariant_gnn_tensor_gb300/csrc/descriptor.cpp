@@ -262,8 +262,7 @@ extern "C" tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh
     std::vector<Term> tin, tsh, tout;
     if (!parse_irreps(irreps_in, tin) || !parse_irreps(irreps_sh, tsh) || !parse_irreps(irreps_out, tout))
         return TP_ERR_PARSE;
-    if (layout == TP_MUL_IR) return TP_ERR_UNSUPPORTED;
-    if (layout != TP_IR_MUL) return TP_ERR_ARG;
+    if (layout != TP_IR_MUL && layout != TP_MUL_IR) return TP_ERR_ARG;
     // O3 vs SO3 must agree across the three strings
     auto kind = [](const std::vector<Term> &v) { return v[0].p != 0; };
     if (kind(tin) != kind(tsh) || kind(tin) != kind(tout)) return TP_ERR_PARSE;
@@ -274,6 +273,7 @@ extern "C" tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh
     std::memset(d, 0, sizeof(*d));
     static std::atomic<uint64_t> next_uid{1};
     d->uid = next_uid.fetch_add(1);
+    d->layout = (int)layout;
     d->n_in = (int)tin.size();
     d->n_sh = (int)tsh.size();
     d->n_out = (int)tout.size();
@@ -393,6 +393,7 @@ extern "C" tp_status tp_desc_query(const tp_desc *d, tp_desc_info *info) {
     info->n_in = d->n_in; info->n_sh = d->n_sh; info->n_out = d->n_out;
     info->lmax_in = d->lmax_in; info->lmax_sh = d->lmax_sh; info->lmax_out = d->lmax_out;
     info->cg_nnz = d->tab.nnz;
+    info->layout = d->layout;
     return TP_OK;
 }
 

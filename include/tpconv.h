@@ -101,6 +101,7 @@ typedef struct {
     int32_t n_in, n_sh, n_out; /* number of blocks */
     int32_t lmax_in, lmax_sh, lmax_out;
     int32_t cg_nnz;        /* nonzero Clebsch-Gordan entries over all paths */
+    int32_t layout;        /* tp_layout of x and out rows */
 } tp_desc_info;
 
 typedef struct {
@@ -113,8 +114,13 @@ typedef struct {
  * Lesson 12a, section 21.2). The host derives the path table, the real
  * Clebsch-Gordan tensors (Racah's formula in the complex basis, then the
  * complex-to-real change of basis) and the kernel tables.
+ * `layout` is the layout of the x and out rows the caller passes (Lesson 12a,
+ * section 21.3): TP_IR_MUL, which every entry point takes, or TP_MUL_IR,
+ * which tp_conv_forward_ex converts blockwise on the device (the kernels
+ * compute in ir_mul); the other entry points return TP_ERR_UNSUPPORTED for a
+ * TP_MUL_IR descriptor.
  * Errors: TP_ERR_PARSE for a malformed string; TP_ERR_UNSUPPORTED when
- * layout != TP_IR_MUL, a degree exceeds 3, a harmonic block has mul != 1,
+ * a degree exceeds 3, a harmonic block has mul != 1,
  * input/output multiplicities differ or are not one value, an output type
  * repeats, two input (or output) blocks share a degree, mul is not a
  * multiple of 8 or exceeds 128, or no path exists; TP_ERR_ARG for nulls.
@@ -254,6 +260,61 @@ TPCONV_API tp_status tp_conv_forward_mlp(const tp_desc *desc, tp_dtype dtype, co
                                          int32_t normalize, const tp_radial_mlp *mlp, const int32_t *src,
                                          const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
                                          float *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Reductions over a destination's incoming edges ("cuEquivariance in PyTorch",
+ * Other operations and layers: the convolution layer supports reduce="mean").
+ * SUM: the formula at the top of this file; MEAN: that sum divided by the
+ * destination's number of edges (destinations without edges stay zero). */
+#define TP_REDUCE_SUM 0
+#define TP_REDUCE_MEAN 1
+
+/* Arguments of tp_conv_forward_ex. The harmonics come either as rows `sh`
+ * [E][dim_sh] or, with `vec` [E][3] non-NULL instead, are evaluated in the
+ * kernel (as tp_conv_forward_vec; `normalize` as there); with `mlp` (needs
+ * `vec`) the weights come from the radial network (as tp_conv_forward_mlp) and
+ * `w` is ignored. x and out rows are in the descriptor's layout; src
+ * [E] and row_ptr [N_dst+1] are int32 (index_bits 32) or int64 (index_bits 64,
+ * "cuEquivariance in PyTorch", SegmentedPolynomial: gather and scatter: index
+ * tensors may be int32 or int64; values must fit int32). The workspace (256-byte
+ * aligned, tp_conv_forward_ex_workspace_size bytes) is required. */
+typedef struct {
+    tp_dtype dtype;
+    const void *x;
+    const float *sh;
+    const float *vec;
+    int32_t normalize;
+    const tp_radial_mlp *mlp;
+    const void *w;
+    const void *src;
+    const void *row_ptr;
+    int32_t index_bits;
+    int32_t reduce;
+    int32_t N_src, N_dst;
+    int64_t E;
+    float *out;
+    void *workspace;
+    size_t workspace_bytes;
+} tp_forward_args;
+
+/* The forward with int64 indices, a TP_MUL_IR descriptor or TP_REDUCE_MEAN.
+ * Around the same fused kernels it runs, on `stream`: int64 -> int32 copies of
+ * src and row_ptr (an index outside int32 becomes -1, which the kernels flag
+ * and skip); a blockwise mul_ir -> ir_mul copy of x and an ir_mul -> mul_ir copy
+ * of out; the mean scaling of each row. Errors as tp_conv_forward, plus
+ * TP_ERR_ARG for a missing or small workspace, both sh and vec, or a bad
+ * index_bits / reduce. */
+TPCONV_API tp_status tp_conv_forward_ex_workspace_size(const tp_desc *desc, const tp_forward_args *args,
+                                                       size_t *bytes);
+TPCONV_API tp_status tp_conv_forward_ex(const tp_desc *desc, const tp_forward_args *args, void *stream);
+
+/* Blockwise layout conversion of `rows` feature rows of the descriptor's input
+ * (which = 0) or output (which = 1) irreps between mul_ir and ir_mul (Lesson
+ * 12a, section 21.3; "cuEquivariance in PyTorch", Layouts and weights: the
+ * conversion is per irrep block, not of the whole flattened row). `from` is the
+ * layout of src; dst receives the other one. src and dst: device, elem_bytes
+ * 2 or 4 per element, distinct, [rows][dim]. */
+TPCONV_API tp_status tp_transpose_layout(const tp_desc *desc, int32_t which, tp_layout from, const void *src,
+                                         void *dst, int64_t rows, int32_t elem_bytes, void *stream);
 
 /* Backward pass of tp_conv_forward (float32), the exact gradients of
  * <grad_out, out> with respect to x, w and sh ("cuEquivariance in PyTorch",

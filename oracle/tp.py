@@ -178,6 +178,16 @@ def conv_forward(plan: Plan, x, sh, w, src, dst, n_dst: int) -> np.ndarray:
     return out
 
 
+def conv_forward_mean(plan: Plan, x, sh, w, src, dst, n_dst: int) -> np.ndarray:
+    """reduce="mean" ("cuEquivariance in PyTorch", Other operations and layers:
+    the convolution layer's mean reduction): the sum of a destination's
+    messages divided by its number of incoming edges; destinations without
+    edges stay zero."""
+    out = conv_forward(plan, x, sh, w, src, dst, n_dst)
+    deg = np.bincount(np.asarray(dst, dtype=np.int64), minlength=n_dst)
+    return out / np.maximum(deg, 1)[:, None]
+
+
 def conv_backward(plan: Plan, x, sh, w, src, dst, g):
     """Exact gradients (dx, dw, dsh) of <g, conv_forward(x, sh, w)>."""
     E = len(src)

@@ -312,3 +312,26 @@ def test_radial_mlp_structure():
     ba, bb = rng.standard_normal(numel), rng.standard_normal(numel)
     np.testing.assert_allclose(tp.radial_mlp(vec, w1, b1, wa + wb, ba + bb),
                                tp.radial_mlp(vec, w1, b1, wa, ba) + tp.radial_mlp(vec, w1, b1, wb, bb), rtol=1e-12)
+
+
+def test_mean_reduction_special_cases():
+    """reduce="mean": every edge of a destination carrying the same message
+    gives that message; one edge gives the sum; destinations without edges stay
+    zero; sum = mean x (number of edges)."""
+    plan = tp.Plan("4x0e+4x1o", "0e+1o+2e", "4x0e+4x1o+4x2e")
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((3, plan.dim_in))
+    vec = rng.standard_normal((1, 3))
+    sh1 = so3.sh_concat([0, 1, 2], vec)
+    w1 = rng.standard_normal((1, plan.weight_numel))
+    # destination 0: five copies of one edge; destination 1: one other edge; 2: none
+    src = np.array([2, 2, 2, 2, 2, 0])
+    dst = np.array([0, 0, 0, 0, 0, 1])
+    sh = np.repeat(sh1, 6, axis=0)
+    w = np.repeat(w1, 6, axis=0)
+    mean = tp.conv_forward_mean(plan, x, sh, w, src, dst, 3)
+    single = tp.conv_forward(plan, x, sh[:1], w[:1], src[:1], np.array([0]), 1)[0]
+    np.testing.assert_allclose(mean[0], single, rtol=1e-13)
+    np.testing.assert_allclose(mean[1], tp.conv_forward(plan, x, sh, w, src, dst, 3)[1], rtol=0, atol=0)
+    assert not np.any(mean[2])
+    np.testing.assert_allclose(5 * mean[0], tp.conv_forward(plan, x, sh, w, src, dst, 3)[0], rtol=1e-13)
