@@ -38,7 +38,7 @@ TP_F32, TP_BF16_IN_F32_OUT = 0, 1
 TP_IR_MUL, TP_MUL_IR = 0, 1
 TP_DEV_ERR_INDEX, TP_DEV_ERR_TIMEOUT, TP_DEV_ERR_SEGMENT = 1, 2, 4
 TP_REDUCE_SUM, TP_REDUCE_MEAN = 0, 1
-EXPORTS = ["tp_desc_create", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
+EXPORTS = ["tp_desc_create", "tp_desc_create_unsimplified", "tp_desc_query", "tp_desc_path", "tp_desc_cg", "tp_desc_destroy",
            "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
            "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
            "tp_conv_forward_vec", "tp_conv_forward_mlp", "tp_conv_forward_ex_workspace_size", "tp_conv_forward_ex",
@@ -87,6 +87,8 @@ class _Path(ctypes.Structure):
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 _sigs = {
     "tp_desc_create": [ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(_vp)],
+    "tp_desc_create_unsimplified": [ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p, ctypes.c_int,
+                                    ctypes.POINTER(_vp)],
     "tp_desc_query": [_vp, ctypes.POINTER(_Info)],
     "tp_desc_path": [_vp, _i32, ctypes.POINTER(_Path)],
     "tp_desc_cg": [_vp, _i32, _vp, _i64],
@@ -164,6 +166,14 @@ def tp_desc_create(irreps_in: str, irreps_sh: str, irreps_out: str, layout: str 
     h = _vp()
     _check(_lib.tp_desc_create(irreps_in.encode(), irreps_sh.encode(), irreps_out.encode(), lay, ctypes.byref(h)),
            "tp_desc_create")
+    return Descriptor(h.value, (irreps_in, irreps_sh, irreps_out))
+
+
+def tp_desc_create_unsimplified(irreps_in: str, irreps_sh: str, irreps_out: str) -> Descriptor:
+    """Descriptor with one output block per path (grouped by output type)."""
+    h = _vp()
+    _check(_lib.tp_desc_create_unsimplified(irreps_in.encode(), irreps_sh.encode(), irreps_out.encode(), TP_IR_MUL,
+                                            ctypes.byref(h)), "tp_desc_create_unsimplified")
     return Descriptor(h.value, (irreps_in, irreps_sh, irreps_out))
 
 

@@ -21,6 +21,9 @@ int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
 size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
 cudaError_t indices_to_i32(const int64_t *in, int64_t n, int32_t *out, cudaStream_t stream);
+cudaError_t unsimp_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
+                           const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
+                           float *out, int sms, int smem_optin, int *status, cudaStream_t stream);
 cudaError_t transpose_rows(const tp_desc *d, int which, int from, const void *src, void *dst, int64_t rows,
                            int elem_bytes, cudaStream_t stream);
 cudaError_t scale_rows_by_inverse_degree(float *out, const int32_t *row_ptr, int32_t n, int32_t dim,
@@ -256,6 +259,14 @@ tp_status forward_core(const tp_desc *desc, const FwdArgs &a, cudaStream_t strea
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
+    if (desc->unsimp) {  // one output block per path: its own kernel (harmonic rows only)
+        if (a.vec_mode != 0 || a.mlp) return TP_ERR_UNSUPPORTED;
+        const cudaError_t eu = unsimp_forward(desc, a.dtype, a.x, a.sh, a.w, a.src, a.row_ptr, a.N_src, a.N_dst, a.E,
+                                              a.out, dev.sms, dev.smem_optin, dev.status, stream);
+        if (eu == cudaSuccess) return TP_OK;
+        (void)cudaGetLastError();
+        return eu == cudaErrorNotSupported ? TP_ERR_UNSUPPORTED : TP_ERR_CUDA;
+    }
     cudaError_t e = cudaErrorNotSupported;
     if (a.vec_mode == 0)  // bfloat16 harmonic rows: the tensor-core kernel first
         e = mma_forward(desc, a.dtype, a.x, a.sh, w, a.src, a.row_ptr, a.N_src, a.N_dst, a.E, a.out, a.ws, a.ws_bytes,
@@ -382,6 +393,7 @@ extern "C" tp_status tp_conv_forward_ex(const tp_desc *desc, const tp_forward_ar
     if (!a->out || !a->row_ptr || (a->E > 0 && (!a->x || !a->src))) return TP_ERR_ARG;
     if (a->sh && a->vec) return TP_ERR_ARG;  // harmonic rows or edge vectors, not both
     if (a->mlp && !a->vec) return TP_ERR_UNSUPPORTED;
+    if (desc->unsimp && a->reduce != TP_REDUCE_SUM) return TP_ERR_UNSUPPORTED;
     DevInfo dev;
     st = dev_info(dev);
     if (st != TP_OK) return st;
@@ -439,7 +451,7 @@ extern "C" tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out
                                       const int32_t *src_perm, const int32_t *src_row_ptr, int32_t N_src,
                                       int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh, void *stream) {
     if (!desc || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
-    if (desc->layout != TP_IR_MUL) return TP_ERR_UNSUPPORTED;
+    if (desc->layout != TP_IR_MUL || desc->unsimp) return TP_ERR_UNSUPPORTED;
     if ((N_src > 0 && (!dx || !src_row_ptr)) || (N_dst > 0 && !row_ptr)) return TP_ERR_ARG;
     if (E > 0 && (!grad_out || !x || !sh || !w || !src || !dst || !src_perm || !dw || !dsh)) return TP_ERR_ARG;
     if (E > 0 && (N_src == 0 || N_dst == 0)) return TP_ERR_INDEX;

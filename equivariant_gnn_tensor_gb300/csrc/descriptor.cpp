@@ -382,15 +382,35 @@ extern "C" tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh
     return TP_OK;
 }
 
+extern "C" tp_status tp_desc_create_unsimplified(const char *irreps_in, const char *irreps_sh,
+                                                 const char *irreps_out, tp_layout layout, tp_desc **out) {
+    if (layout != TP_IR_MUL) return TP_ERR_UNSUPPORTED;
+    tp_status st = tp_desc_create(irreps_in, irreps_sh, irreps_out, layout, out);
+    if (st != TP_OK) return st;
+    tp_desc *d = *out;
+    // blocks grouped by output type in the order of the output list, paths of one type in path order
+    int off = 0, pos = 0;
+    for (int c = 0; c < d->n_out; ++c)
+        for (int p = 0; p < d->n_paths; ++p) {
+            if (d->path_c[p] != c) continue;
+            d->unsimp_off[p] = off;
+            d->unsimp_block[p] = pos++;
+            off += d->tab.mul * (2 * d->out_l[c] + 1);
+        }
+    d->unsimp_dim_out = off;
+    d->unsimp = 1;
+    return TP_OK;
+}
+
 extern "C" tp_status tp_desc_query(const tp_desc *d, tp_desc_info *info) {
     if (!d || !info) return TP_ERR_ARG;
     info->n_paths = d->n_paths;
     info->mul = d->tab.mul;
     info->dim_x = d->tab.dim_x;
     info->dim_sh = d->tab.dim_sh;
-    info->dim_out = d->tab.dim_out;
+    info->dim_out = d->unsimp ? d->unsimp_dim_out : d->tab.dim_out;
     info->weight_numel = d->tab.wnum;
-    info->n_in = d->n_in; info->n_sh = d->n_sh; info->n_out = d->n_out;
+    info->n_in = d->n_in; info->n_sh = d->n_sh; info->n_out = d->unsimp ? d->n_paths : d->n_out;
     info->lmax_in = d->lmax_in; info->lmax_sh = d->lmax_sh; info->lmax_out = d->lmax_out;
     info->cg_nnz = d->tab.nnz;
     info->layout = d->layout;
@@ -401,6 +421,7 @@ extern "C" tp_status tp_desc_path(const tp_desc *d, int32_t p, tp_path_info *inf
     if (!d || !info || p < 0 || p >= d->n_paths) return TP_ERR_ARG;
     info->a = d->path_a[p]; info->b = d->path_b[p]; info->c = d->path_c[p];
     info->la = d->in_l[info->a]; info->lb = d->sh_l[info->b]; info->lc = d->out_l[info->c];
+    if (d->unsimp) info->c = d->unsimp_block[p];
     return TP_OK;
 }
 

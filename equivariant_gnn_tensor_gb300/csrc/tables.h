@@ -64,6 +64,10 @@ void launch_cache_forget(uint64_t uid);
 struct tp_desc {
     uint64_t uid;  // unique per descriptor created in this process (launch-plan cache key)
     int layout;    // tp_layout of the feature rows the caller passes (the kernels compute in ir_mul)
+    int unsimp;    // one output block per path (tp_desc_create_unsimplified)
+    int unsimp_dim_out;                 // sum over paths of mul*(2lc+1)
+    int unsimp_off[tpc::kMaxPaths];     // offset of path p's output block
+    int unsimp_block[tpc::kMaxPaths];   // position of path p's block in the output listing
     // parsed irreps: (mul, l, parity) with parity +1/-1 (O3) or 0 (SO3)
     int n_in, n_sh, n_out;
     int in_mul[8], in_l[8], in_p[8];

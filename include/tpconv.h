@@ -127,6 +127,18 @@ typedef struct {
  * On success *out owns host memory until tp_desc_destroy. */
 TPCONV_API tp_status tp_desc_create(const char *irreps_in, const char *irreps_sh, const char *irreps_out,
                          tp_layout layout, tp_desc **out);
+/* A descriptor whose output has one block per path ("unsimplified", as the
+ * descriptor printout of Lesson 12a, section 21.4: 32x0e+32x1o x 0e+1o gives
+ * D=32x0e+32x0e+32x1o+32x1o) instead of one per output type: irreps_out
+ * lists the allowed output types; path p writes its own block of
+ * mul*(2l_c+1) elements; blocks are grouped by output type in the order of
+ * irreps_out, paths of one type in path order. tp_desc_query reports that
+ * output width and n_out = n_paths; tp_desc_path reports a path's block as c.
+ * tp_conv_forward (and tp_conv_forward_ex with reduce sum, int32 or int64
+ * indices) accept it; layout must be TP_IR_MUL, and every other entry point
+ * returns TP_ERR_UNSUPPORTED for it. */
+TPCONV_API tp_status tp_desc_create_unsimplified(const char *irreps_in, const char *irreps_sh,
+                                                 const char *irreps_out, tp_layout layout, tp_desc **out);
 TPCONV_API tp_status tp_desc_query(const tp_desc *desc, tp_desc_info *info);
 /* Path p in enumeration order (the weight layout order). */
 TPCONV_API tp_status tp_desc_path(const tp_desc *desc, int32_t p, tp_path_info *info);

@@ -178,6 +178,32 @@ def conv_forward(plan: Plan, x, sh, w, src, dst, n_dst: int) -> np.ndarray:
     return out
 
 
+def unsimplified_order(plan: Plan) -> list[int]:
+    """Path indices in the order of the per-path ("unsimplified") output blocks:
+    grouped by output irrep type in the order of the output list, paths of one
+    type in path order (Lesson 12a, section 21.4: the descriptor of
+    32x0e+32x1o x 0e+1o prints D=32x0e+32x0e+32x1o+32x1o)."""
+    return [p for c in range(len(plan.irr_out)) for p, P in enumerate(plan.paths) if P.c == c]
+
+
+def conv_forward_unsimplified(plan: Plan, x, sh, w, src, dst, n_dst: int) -> np.ndarray:
+    """Gather, contract, sum-scatter with one output block of mul*(2 l_c + 1)
+    per path (in ``unsimplified_order``) instead of one per output type."""
+    E = len(src)
+    mul = plan.mul
+    xs = x[src]
+    blocks = []
+    for p in unsimplified_order(plan):
+        P = plan.paths[p]
+        t = np.einsum("ijk,eiu,ej->eku", plan.cg[p], plan.xblock(xs, P.a), plan.shblock(sh, P.b))
+        t *= w[:, None, p * mul:(p + 1) * mul]
+        blocks.append(t.reshape(E, (2 * P.lc + 1) * mul))
+    m = np.concatenate(blocks, axis=1) if blocks else np.zeros((E, 0))
+    out = np.zeros((n_dst, m.shape[1]))
+    np.add.at(out, np.asarray(dst, dtype=np.int64), m)
+    return out
+
+
 def conv_forward_mean(plan: Plan, x, sh, w, src, dst, n_dst: int) -> np.ndarray:
     """reduce="mean" ("cuEquivariance in PyTorch", Other operations and layers:
     the convolution layer's mean reduction): the sum of a destination's

@@ -138,3 +138,33 @@ def test_all_variants_together(tpc):
     ref = tp.conv_forward_mean(plan, rounded(prob["x"], torch.float32), prob["sh"], prob["w"], prob["src"],
                                prob["dst"], prob["n_dst"])
     assert err(out, I.convert_layout(ref, plan.irr_out, "ir_mul", "mul_ir")) <= FP32_TOL
+
+
+@pytest.mark.parametrize("irr", [("32x0e+32x1o", "0e+1o", "32x0e+32x1o")] + SHAPES, ids=["lesson"] + IDS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_unsimplified_outputs(tpc, irr, dtype):
+    """One output block per path (tp_desc_create_unsimplified) against the
+    oracle's per-path blocks, with empty destinations and int32 / int64 indices."""
+    rng = np.random.default_rng(77)
+    dst = rng.integers(0, 120, 2500) * 2
+    prob = make_problem(*irr, n_src=200, n_dst=241, E=len(dst), seed=78, dst=dst)
+    plan = prob["plan"]
+    desc = tpc.tp_desc_create_unsimplified(*irr)
+    order = tp.unsimplified_order(plan)
+    assert desc.n_out == plan.n_paths and desc.dim_out == sum(plan.mul * (2 * plan.paths[p].lc + 1) for p in order)
+    for pos, p in enumerate(order):
+        assert tpc.tp_desc_path(desc, p)[2] == pos
+    g = gpu_sorted_inputs(tpc, prob, dtype)
+    out = tpc.tp_conv_forward(desc, g["x"], g["sh"], g["w"], g["src"], g["row_ptr"], prob["n_dst"])
+    out64 = tpc.tp_conv_forward_ex(desc, g["x"], g["src"].long(), g["row_ptr"].long(), prob["n_dst"], w=g["w"],
+                                   sh=g["sh"])
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+    ref = tp.conv_forward_unsimplified(plan, rounded(prob["x"], dtype), rounded(prob["sh"], torch.float32),
+                                       rounded(prob["w"], dtype), prob["src"], prob["dst"], prob["n_dst"])
+    assert err(out, ref) <= FP32_TOL
+    assert torch.equal(out, out64)
+    with pytest.raises(tpc.TPError):   # the backward has no per-path outputs
+        sp, srp, _ = tpc.tp_csr_build(g["src"], prob["n_src"])
+        tpc.tp_conv_backward(desc, out, g["x"].float(), g["sh"], g["w"].float(), g["src"], g["dst"], g["row_ptr"],
+                             sp, srp)

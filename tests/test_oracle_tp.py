@@ -335,3 +335,27 @@ def test_mean_reduction_special_cases():
     np.testing.assert_allclose(mean[1], tp.conv_forward(plan, x, sh, w, src, dst, 3)[1], rtol=0, atol=0)
     assert not np.any(mean[2])
     np.testing.assert_allclose(5 * mean[0], tp.conv_forward(plan, x, sh, w, src, dst, 3)[0], rtol=1e-13)
+
+
+def test_unsimplified_outputs():
+    """Per-path output blocks: their listing for the lesson's example is the
+    printed D=32x0e+32x0e+32x1o+32x1o, and adding the blocks of one output type
+    gives the simplified output."""
+    g = GOLD["channelwise_32x0e32x1o_sh_0e1o"]
+    plan = tp.Plan(g["irreps_in"], g["irreps_sh"], g["irreps_out"])
+    order = tp.unsimplified_order(plan)
+    listing = "+".join(str(I.MulIrrep(plan.mul, plan.paths[p].lc, plan.irr_out[plan.paths[p].c].p)) for p in order)
+    assert listing == g["path_outputs_unsimplified"]
+    for irr in [("4x0e+4x1o", "0e+1o+2e", "4x0e+4x1o+4x2e"), ("8x0e+8x1o+8x2e", "0e+1o+2e+3o", "8x0e+8x1o+8x2e")]:
+        plan = tp.Plan(*irr)
+        _, x, _, sh, w, src, dst = random_problem(*irr, n_src=9, n_dst=7, E=40, seed=3)
+        un = tp.conv_forward_unsimplified(plan, x, sh, w, src, dst, 7)
+        simp = np.zeros((7, plan.dim_out))
+        col = 0
+        for p in tp.unsimplified_order(plan):
+            P = plan.paths[p]
+            width = (2 * P.lc + 1) * plan.mul
+            simp[:, plan.oblock_slice(P.c)] += un[:, col:col + width]
+            col += width
+        assert col == un.shape[1]
+        np.testing.assert_allclose(simp, tp.conv_forward(plan, x, sh, w, src, dst, 7), atol=1e-12)
