@@ -397,6 +397,43 @@ class Forward:
         return e0.elapsed_time(e1), h2d, d2h
 
 
+def symmetric_contraction_bench(tpc, torch, device, stream, peak, peak_src, local, steps: int = 500):
+    """The symmetric contraction of the lesson's MACE descriptor (32x0e+32x1o
+    -> 32x0e, degrees 1..3) on N=1048576 nodes with 10 elements (x: 512 MiB,
+    larger than L2): per step one read of x and the element indices, one
+    write of out (the weights stay in L1/L2)."""
+    N, n_el = 1048576, 10
+    s = tpc.tp_symc_create("32x0e+32x1o", "32x0e", 3)
+    g = torch.Generator(device=device).manual_seed(11)
+    x = torch.randn((N, s.dim_in), device=device, generator=g)
+    w = torch.randn((n_el, s.n_weights, s.mul), device=device, generator=g)
+    el = torch.randint(0, n_el, (N,), device=device, dtype=torch.int32, generator=g)
+    out = torch.empty((N, s.dim_out), device=device)
+    for _ in range(5):
+        tpc.tp_symmetric_contraction(s, x, w, el, out=out, stream=stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        tpc.tp_symmetric_contraction(s, x, w, el, out=out, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = sampler.stop()
+    if tpc.tp_device_status(reset=True) != 0:
+        raise RuntimeError("device status set during the symmetric contraction timing")
+    us = e0.elapsed_time(e1) / steps * 1e3
+    nbytes = N * (s.dim_in + s.dim_out + 1) * 4 + n_el * s.n_weights * s.mul * 4
+    ach = nbytes / (us * 1e-6) / 1e9
+    return {"workload": f"symmetric contraction 32x0e+32x1o -> 32x0e, degrees 1..3, N={N}, {n_el} elements (fp32)",
+            "value": N / (us * 1e-6), "unit": "nodes/s", "steps": steps, "kernel_us": us,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                         "traffic": None, "algorithmic_bytes": nbytes, "kernel_us": us, "peak_source": peak_src},
+            "clocks": clk, "gpu_launches": steps}
+
+
 def tiny_latency(tpc, torch, device, stream, calls: int = 20000):
     """The tiny workload (512 edges) is launch-bound: per-call device time
     (CUDA events over back-to-back calls) and per-call host time of the public
@@ -565,6 +602,7 @@ def bench_ours(args):
             del g
             torch.cuda.empty_cache()
         line["configs"] = cfgs
+        line["symmetric_contraction"] = symmetric_contraction_bench(tpc, torch, device, stream, peak, peak_src, local)
         if not args.no_backward:
             # the fwd+bwd workload: the medium graph and features with its own grad_out
             b = Forward("fwdbwd", args.seed, tpc, torch, device, stream)

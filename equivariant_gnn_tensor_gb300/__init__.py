@@ -42,7 +42,8 @@ EXPORTS = ["tp_desc_create", "tp_desc_create_unsimplified", "tp_desc_query", "tp
            "tp_spherical_harmonics", "tp_csr_workspace_size", "tp_csr_build", "tp_csr_build_noalloc",
            "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
            "tp_conv_forward_vec", "tp_conv_forward_mlp", "tp_conv_forward_ex_workspace_size", "tp_conv_forward_ex",
-           "tp_transpose_layout",
+           "tp_transpose_layout", "tp_symc_create", "tp_symc_query", "tp_symc_term", "tp_symc_destroy",
+           "tp_symmetric_contraction",
            "tp_conv_backward", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
            "tp_abi_version"]
 
@@ -80,6 +81,11 @@ class _FwdArgs(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t)]
 
 
+class _SymcInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("mul", "dim_in", "dim_out", "max_degree", "n_weights", "n_terms")] + \
+        [("num_paths", ctypes.c_int32 * 3), ("weights_per_degree", ctypes.c_int32 * 3)]
+
+
 class _Path(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("a", "b", "c", "la", "lb", "lc")]
 
@@ -104,6 +110,10 @@ _sigs = {
     "tp_conv_forward_ex_workspace_size": [_vp, ctypes.POINTER(_FwdArgs), ctypes.POINTER(_sz)],
     "tp_conv_forward_ex": [_vp, ctypes.POINTER(_FwdArgs), _vp],
     "tp_transpose_layout": [_vp, _i32, ctypes.c_int, _vp, _vp, _i64, _i32, _vp],
+    "tp_symc_create": [ctypes.c_char_p, ctypes.c_char_p, _i32, ctypes.POINTER(_vp)],
+    "tp_symc_query": [_vp, ctypes.POINTER(_SymcInfo)],
+    "tp_symc_term": [_vp, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp, _i64],
+    "tp_symmetric_contraction": [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp],
     "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
     "tp_set_tuning": [ctypes.POINTER(_Tuning)],
@@ -114,6 +124,8 @@ for _n, _a in _sigs.items():
     getattr(_lib, _n).restype = ctypes.c_int
 _lib.tp_desc_destroy.argtypes = [_vp]
 _lib.tp_desc_destroy.restype = None
+_lib.tp_symc_destroy.argtypes = [_vp]
+_lib.tp_symc_destroy.restype = None
 _lib.tp_status_string.argtypes = [ctypes.c_int]
 _lib.tp_status_string.restype = ctypes.c_char_p
 _lib.tp_csr_build_noalloc_max_edges.argtypes = []
@@ -151,6 +163,62 @@ class Descriptor:
     def __repr__(self):
         return (f"Descriptor({self.irreps_in!r} x {self.irreps_sh!r} -> {self.irreps_out!r}, "
                 f"paths={self.n_paths}, weight_numel={self.weight_numel})")
+
+
+class SymcDescriptor:
+    """Owns a tp_symc (host memory); fields mirror tp_symc_info."""
+
+    def __init__(self, handle: int, irreps_in: str, irreps_out: str):
+        self._h = _vp(handle)
+        self.irreps_in, self.irreps_out = irreps_in, irreps_out
+        info = _SymcInfo()
+        _check(_lib.tp_symc_query(self._h, ctypes.byref(info)), "tp_symc_query")
+        for f in ("mul", "dim_in", "dim_out", "max_degree", "n_weights", "n_terms"):
+            setattr(self, f, int(getattr(info, f)))
+        self.num_paths = list(info.num_paths)[:self.max_degree]
+        self.weights_per_degree = list(info.weights_per_degree)[:self.max_degree]
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            _lib.tp_symc_destroy(h)
+            self._h = _vp(0)
+
+
+def tp_symc_create(irreps_in: str, irreps_out: str, max_degree: int) -> SymcDescriptor:
+    h = _vp()
+    _check(_lib.tp_symc_create(irreps_in.encode(), irreps_out.encode(), max_degree, ctypes.byref(h)), "tp_symc_create")
+    return SymcDescriptor(h.value, irreps_in, irreps_out)
+
+
+def tp_symc_query(symc: SymcDescriptor) -> dict:
+    return {f: getattr(symc, f) for f in ("mul", "dim_in", "dim_out", "max_degree", "n_weights", "n_terms",
+                                          "num_paths", "weights_per_degree")}
+
+
+def tp_symc_term(symc: SymcDescriptor, t: int, D: int, out_dim: int = None):
+    """(nu, output block, basis [n_q, D, .., D, 2L+1] float64) of term t; D is
+    the number of input components per channel."""
+    nu, c, nq = _i32(), _i32(), _i32()
+    _check(_lib.tp_symc_term(symc.handle, t, ctypes.byref(nu), ctypes.byref(c), ctypes.byref(nq), None, 0),
+           "tp_symc_term")
+    return int(nu.value), int(c.value), int(nq.value)
+
+
+def tp_symc_basis(symc: SymcDescriptor, t: int, D: int, K: int) -> np.ndarray:
+    nu, c, nq = tp_symc_term(symc, t, D)
+    arr = np.zeros((nq,) + (D,) * nu + (K,), dtype=np.float64)
+    _check(_lib.tp_symc_term(symc.handle, t, ctypes.byref(_i32()), ctypes.byref(_i32()), ctypes.byref(_i32()),
+                             arr.ctypes.data_as(_vp), arr.size), "tp_symc_term")
+    return arr
+
+
+def tp_symc_destroy(symc: SymcDescriptor):
+    symc.__del__()
 
 
 def tp_abi_version() -> int:
@@ -474,6 +542,21 @@ def tp_get_tuning() -> dict:
     t = _Tuning()
     _check(_lib.tp_get_tuning(ctypes.byref(t)), "tp_get_tuning")
     return {f: int(getattr(t, f)) for f in TUNING_FIELDS}
+
+
+def tp_symmetric_contraction(symc: SymcDescriptor, x, weights, element, out=None, stream=None):
+    """out [N, dim_out] float32 of the symmetric contraction of x [N, dim_in]
+    with weights [num_elements, n_weights, mul] selected by element [N] int32."""
+    torch = _torch()
+    N = x.shape[0]
+    if out is None:
+        out = torch.empty((N, symc.dim_out), dtype=torch.float32, device=x.device)
+    f = torch.float32
+    _check(_lib.tp_symmetric_contraction(symc.handle, _dev_ptr(x, "x", f, 2), _dev_ptr(weights, "weights", f, 3),
+                                         _dev_ptr(element, "element", torch.int32, 1), N, weights.shape[0],
+                                         _dev_ptr(out, "out", f, 2), _stream(stream)),
+           "tp_symmetric_contraction")
+    return out
 
 
 def tp_device_status(reset: bool = True, stream=None) -> int:

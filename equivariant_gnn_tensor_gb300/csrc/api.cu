@@ -21,6 +21,8 @@ int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
 size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
 cudaError_t indices_to_i32(const int64_t *in, int64_t n, int32_t *out, cudaStream_t stream);
+cudaError_t symc_launch(const tp_symc *s, const float *x, const float *weights, const int32_t *element, int32_t N,
+                        int32_t num_elements, float *out, int sms, int smem_optin, int *status, cudaStream_t stream);
 cudaError_t unsimp_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
                            const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
                            float *out, int sms, int smem_optin, int *status, cudaStream_t stream);
@@ -542,6 +544,24 @@ extern "C" tp_status tp_get_tuning(tp_tuning *t) {
     if (!t) return TP_ERR_ARG;
     *t = tuning_snapshot().t;
     return TP_OK;
+}
+
+extern "C" tp_status tp_symmetric_contraction(const tp_symc *symc, const float *x, const float *weights,
+                                              const int32_t *element, int32_t N, int32_t num_elements, float *out,
+                                              void *stream) {
+    if (!symc || N < 0 || num_elements < 1) return TP_ERR_ARG;
+    if (N == 0) return TP_OK;
+    if (!x || !weights || !element || !out) return TP_ERR_ARG;
+    if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(weights) & 7u) || !aligned4(element))
+        return TP_ERR_ALIGN;
+    DevInfo dev;
+    tp_status st = dev_info(dev);
+    if (st != TP_OK) return st;
+    const cudaError_t e = symc_launch(symc, x, weights, element, N, num_elements, out, dev.sms, dev.smem_optin,
+                                      dev.status, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) return TP_OK;
+    (void)cudaGetLastError();
+    return e == cudaErrorNotSupported ? TP_ERR_UNSUPPORTED : TP_ERR_CUDA;
 }
 
 extern "C" tp_status tp_device_status(int32_t *flags, int32_t reset, void *stream) {

@@ -148,6 +148,9 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
+// Close this thread's open group of cp.async copies.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
 // Wait until at most n of this thread's cp.async groups are still pending
 // (n in 0..7; larger n waits for n = 7).
 __device__ __forceinline__ void cp_async_wait_pending(int n) {

@@ -12,6 +12,7 @@
 // which is real up to one global phase; the phase is dropped, the tensor is
 // scaled to be orthonormal over (i,j) for each k and its sign fixed so the
 // first entry above 1e-9 in (i,j,k) row-major order is positive.
+#include <algorithm>
 #include <atomic>
 #include <cctype>
 #include <cmath>
@@ -24,6 +25,7 @@
 
 #include "../../include/tpconv.h"
 #include "program.h"
+#include "symc.h"
 #include "tables.h"
 
 namespace {
@@ -435,3 +437,291 @@ extern "C" tp_status tp_desc_cg(const tp_desc *d, int32_t p, double *out, int64_
 }
 
 extern "C" void tp_desc_destroy(tp_desc *d) { free_desc(d); }
+
+// ---- symmetric contraction: the basis of symmetric equivariant tensors ------------
+//
+// For degree nu and output irrep L, the tensors T[i_1..i_nu, k] over the
+// components of one channel of the input (i over every block) that are
+// symmetric in the nu slots and equivariant. Spanned by the symmetrised
+// coupling trees built from this file's Clebsch-Gordan tensors:
+//   nu = 1: the identity on each block of type L;
+//   nu = 2: C^{l1 l2 L} on blocks (b1, b2) with p1 p2 = pL;
+//   nu = 3: sum_m C^{l1 l2 l12}[i1,i2,m] C^{l12 l3 L}[m,i3,k] for every
+//           intermediate l12, with p1 p2 p3 = pL;
+// each symmetrised over the orderings of its slots. The span is then made
+// canonical: reduced row echelon form of the flattened candidates (row-major
+// over (i_1..i_nu, k)), each row scaled to unit norm, leading entry positive.
+
+struct tp_symc {
+    int mul, n_in, n_out, max_degree;
+    int in_l[8], in_p[8], in_off[8];   // per channel: component offsets (mul 1)
+    int out_l[8], out_p[8], out_off[8];  // output blocks (element offsets, ir_mul)
+    int D, dim_in, dim_out;
+    int n_terms;
+    int term_nu[32], term_c[32], term_nq[32], term_q0[32];
+    std::vector<double> basis[32];     // [nq][D^nu][2L+1]
+    int n_weights;
+    int num_paths[3], weights_per_degree[3];
+    std::vector<tpc::SymcEntry> entries;  // the kernel's table
+};
+
+namespace {
+bool build_symc_entries(tp_symc *s);
+}  // namespace
+
+namespace {
+
+void symmetrise(std::vector<double> &T, int D, int nu, int K) {
+    if (nu == 1) return;
+    std::vector<double> S(T.size(), 0.0);
+    if (nu == 2) {
+        for (int a = 0; a < D; ++a)
+            for (int b = 0; b < D; ++b)
+                for (int k = 0; k < K; ++k) S[(a * D + b) * K + k] = T[(a * D + b) * K + k] + T[(b * D + a) * K + k];
+    } else {
+        const int perm[6][3] = {{0, 1, 2}, {0, 2, 1}, {1, 0, 2}, {1, 2, 0}, {2, 0, 1}, {2, 1, 0}};
+        for (int a = 0; a < D; ++a)
+            for (int b = 0; b < D; ++b)
+                for (int c = 0; c < D; ++c) {
+                    const int idx[3] = {a, b, c};
+                    for (int k = 0; k < K; ++k) {
+                        double v = 0.0;
+                        for (int q = 0; q < 6; ++q)
+                            v += T[((idx[perm[q][0]] * D + idx[perm[q][1]]) * D + idx[perm[q][2]]) * K + k];
+                        S[((a * D + b) * D + c) * K + k] = v;
+                    }
+                }
+    }
+    T.swap(S);
+}
+
+// rows (each of length n) -> canonical basis of their span
+std::vector<std::vector<double>> rref_canonical(std::vector<std::vector<double>> A, size_t n) {
+    size_t r = 0;
+    for (size_t c = 0; c < n && r < A.size(); ++c) {
+        size_t piv = r;
+        for (size_t q = r; q < A.size(); ++q)
+            if (std::fabs(A[q][c]) > std::fabs(A[piv][c])) piv = q;
+        if (std::fabs(A[piv][c]) < 1e-9) continue;
+        std::swap(A[r], A[piv]);
+        const double inv = 1.0 / A[r][c];
+        for (size_t j = 0; j < n; ++j) A[r][j] *= inv;
+        for (size_t q = 0; q < A.size(); ++q) {
+            if (q == r || A[q][c] == 0.0) continue;
+            const double f = A[q][c];
+            for (size_t j = 0; j < n; ++j) A[q][j] -= f * A[r][j];
+        }
+        ++r;
+    }
+    A.resize(r);
+    for (auto &row : A) {
+        double nrm = 0.0, lead = 0.0;
+        for (double &v : row) {
+            if (std::fabs(v) < 1e-12) v = 0.0;
+            nrm += v * v;
+            if (lead == 0.0 && std::fabs(v) > 1e-9) lead = v;
+        }
+        const double s = (lead < 0 ? -1.0 : 1.0) / std::sqrt(nrm);
+        for (double &v : row) v *= s;
+    }
+    return A;
+}
+
+}  // namespace
+
+extern "C" tp_status tp_symc_create(const char *irreps_in, const char *irreps_out, int32_t max_degree,
+                                    tp_symc **out) {
+    if (!irreps_in || !irreps_out || !out || max_degree < 1) return TP_ERR_ARG;
+    *out = nullptr;
+    if (max_degree > 3) return TP_ERR_UNSUPPORTED;
+    std::vector<Term> tin, tout;
+    if (!parse_irreps(irreps_in, tin) || !parse_irreps(irreps_out, tout)) return TP_ERR_PARSE;
+    if ((tin[0].p != 0) != (tout[0].p != 0)) return TP_ERR_PARSE;
+    if (tin.size() > 8 || tout.size() > 8) return TP_ERR_UNSUPPORTED;
+    tp_symc *s = new (std::nothrow) tp_symc();
+    if (!s) return TP_ERR_ARG;
+    s->mul = tin[0].mul;
+    s->max_degree = max_degree;
+    s->n_in = (int)tin.size();
+    s->n_out = (int)tout.size();
+    int D = 0, off = 0;
+    for (int b = 0; b < s->n_in; ++b) {
+        if (tin[b].mul != s->mul || tin[b].l > 2) { delete s; return TP_ERR_UNSUPPORTED; }
+        s->in_l[b] = tin[b].l; s->in_p[b] = tin[b].p; s->in_off[b] = D;
+        D += 2 * tin[b].l + 1;
+    }
+    for (int c = 0; c < s->n_out; ++c) {
+        if (tout[c].mul != s->mul || tout[c].l > 3) { delete s; return TP_ERR_UNSUPPORTED; }
+        s->out_l[c] = tout[c].l; s->out_p[c] = tout[c].p; s->out_off[c] = off;
+        off += s->mul * (2 * tout[c].l + 1);
+    }
+    if (s->mul % 32 != 0) { delete s; return TP_ERR_UNSUPPORTED; }
+    s->D = D;
+    s->dim_in = D * s->mul;
+    s->dim_out = off;
+    auto par_ok = [](int p, int q) { return p == 0 || p == q; };
+    s->n_terms = 0;
+    s->n_weights = 0;
+    for (int nu = 1; nu <= max_degree; ++nu) {
+        s->num_paths[nu - 1] = s->weights_per_degree[nu - 1] = 0;
+        for (int c = 0; c < s->n_out; ++c) {
+            const int L = s->out_l[c], pL = s->out_p[c], K = 2 * L + 1;
+            size_t n = (size_t)K;
+            for (int t = 0; t < nu; ++t) n *= (size_t)D;
+            std::vector<std::vector<double>> cand;
+            auto at3 = [&](int a, int b, int cc, int k) { return (((size_t)a * D + b) * D + cc) * K + k; };
+            if (nu == 1) {
+                for (int b = 0; b < s->n_in; ++b) {
+                    if (s->in_l[b] != L || !par_ok(s->in_p[b], pL)) continue;
+                    std::vector<double> T(n, 0.0);
+                    for (int k = 0; k < K; ++k) T[(size_t)(s->in_off[b] + k) * K + k] = 1.0;
+                    cand.push_back(T);
+                }
+            } else if (nu == 2) {
+                for (int b1 = 0; b1 < s->n_in; ++b1)
+                    for (int b2 = 0; b2 < s->n_in; ++b2) {
+                        const int l1 = s->in_l[b1], l2 = s->in_l[b2];
+                        if (L < std::abs(l1 - l2) || L > l1 + l2 || !par_ok(s->in_p[b1] * s->in_p[b2], pL)) continue;
+                        std::vector<double> C((size_t)(2 * l1 + 1) * (2 * l2 + 1) * K);
+                        real_cg(l1, l2, L, C.data());
+                        std::vector<double> T(n, 0.0);
+                        for (int i = 0; i < 2 * l1 + 1; ++i)
+                            for (int j = 0; j < 2 * l2 + 1; ++j)
+                                for (int k = 0; k < K; ++k)
+                                    T[((size_t)(s->in_off[b1] + i) * D + s->in_off[b2] + j) * K + k] =
+                                        C[((size_t)i * (2 * l2 + 1) + j) * K + k];
+                        symmetrise(T, D, 2, K);
+                        cand.push_back(T);
+                    }
+            } else {
+                for (int b1 = 0; b1 < s->n_in; ++b1)
+                    for (int b2 = 0; b2 < s->n_in; ++b2)
+                        for (int b3 = 0; b3 < s->n_in; ++b3) {
+                            const int l1 = s->in_l[b1], l2 = s->in_l[b2], l3 = s->in_l[b3];
+                            if (!par_ok(s->in_p[b1] * s->in_p[b2] * s->in_p[b3], pL)) continue;
+                            for (int l12 = std::abs(l1 - l2); l12 <= l1 + l2; ++l12) {
+                                if (L < std::abs(l12 - l3) || L > l12 + l3) continue;
+                                const int n12 = 2 * l12 + 1;
+                                std::vector<double> C1((size_t)(2 * l1 + 1) * (2 * l2 + 1) * n12),
+                                    C2((size_t)n12 * (2 * l3 + 1) * K);
+                                real_cg(l1, l2, l12, C1.data());
+                                real_cg(l12, l3, L, C2.data());
+                                std::vector<double> T(n, 0.0);
+                                for (int i = 0; i < 2 * l1 + 1; ++i)
+                                    for (int j = 0; j < 2 * l2 + 1; ++j)
+                                        for (int q = 0; q < 2 * l3 + 1; ++q)
+                                            for (int k = 0; k < K; ++k) {
+                                                double v = 0.0;
+                                                for (int m = 0; m < n12; ++m)
+                                                    v += C1[((size_t)i * (2 * l2 + 1) + j) * n12 + m] *
+                                                         C2[((size_t)m * (2 * l3 + 1) + q) * K + k];
+                                                T[at3(s->in_off[b1] + i, s->in_off[b2] + j, s->in_off[b3] + q, k)] = v;
+                                            }
+                                symmetrise(T, D, 3, K);
+                                cand.push_back(T);
+                            }
+                        }
+            }
+            std::vector<std::vector<double>> B = rref_canonical(cand, n);
+            if (B.empty()) continue;
+            if (s->n_terms >= 32) { delete s; return TP_ERR_UNSUPPORTED; }
+            const int t = s->n_terms++;
+            s->term_nu[t] = nu;
+            s->term_c[t] = c;
+            s->term_nq[t] = (int)B.size();
+            s->term_q0[t] = s->n_weights;
+            s->n_weights += (int)B.size();
+            s->weights_per_degree[nu - 1] += (int)B.size();
+            s->basis[t].assign(B.size() * n, 0.0);
+            for (size_t q = 0; q < B.size(); ++q)
+                for (size_t j = 0; j < n; ++j) {
+                    s->basis[t][q * n + j] = B[q][j];
+                    if (B[q][j] != 0.0) ++s->num_paths[nu - 1];
+                }
+        }
+    }
+    if (s->n_terms == 0 || !build_symc_entries(s)) { delete s; return TP_ERR_UNSUPPORTED; }
+    *out = s;
+    return TP_OK;
+}
+
+extern "C" tp_status tp_symc_query(const tp_symc *s, tp_symc_info *info) {
+    if (!s || !info) return TP_ERR_ARG;
+    info->mul = s->mul;
+    info->dim_in = s->dim_in;
+    info->dim_out = s->dim_out;
+    info->max_degree = s->max_degree;
+    info->n_weights = s->n_weights;
+    info->n_terms = s->n_terms;
+    for (int k = 0; k < 3; ++k) {
+        info->num_paths[k] = k < s->max_degree ? s->num_paths[k] : 0;
+        info->weights_per_degree[k] = k < s->max_degree ? s->weights_per_degree[k] : 0;
+    }
+    return TP_OK;
+}
+
+extern "C" tp_status tp_symc_term(const tp_symc *s, int32_t t, int32_t *nu, int32_t *out_block, int32_t *n_q,
+                                  double *basis, int64_t capacity) {
+    if (!s || t < 0 || t >= s->n_terms || !nu || !out_block || !n_q) return TP_ERR_ARG;
+    *nu = s->term_nu[t];
+    *out_block = s->term_c[t];
+    *n_q = s->term_nq[t];
+    if (basis) {
+        if (capacity < (int64_t)s->basis[t].size()) return TP_ERR_ARG;
+        std::memcpy(basis, s->basis[t].data(), sizeof(double) * s->basis[t].size());
+    }
+    return TP_OK;
+}
+
+extern "C" void tp_symc_destroy(tp_symc *s) { delete s; }
+
+namespace {
+// The nonzero basis entries in weight order (the kernel's table).
+bool build_symc_entries(tp_symc *s) {
+    s->entries.clear();
+    for (int t = 0; t < s->n_terms; ++t) {
+        const int nu = s->term_nu[t], c = s->term_c[t], K = 2 * s->out_l[c] + 1, D = s->D;
+        size_t per = (size_t)K;
+        for (int q = 0; q < nu; ++q) per *= (size_t)D;
+        for (int q = 0; q < s->term_nq[t]; ++q)
+            for (size_t j = 0; j < per; ++j) {
+                const double v = s->basis[t][q * per + j];
+                if (v == 0.0) continue;
+                if ((int)s->entries.size() >= tpc::kSymcMaxEntries) return false;
+                size_t r = j;
+                const int k = (int)(r % K);
+                r /= K;
+                int idx[3] = {0, 0, 0};
+                for (int a = nu - 1; a >= 0; --a) {
+                    idx[a] = (int)(r % D);
+                    r /= D;
+                }
+                tpc::SymcEntry e;
+                e.nu = (uint8_t)nu;
+                e.i1 = (uint8_t)idx[0];
+                e.i2 = (uint8_t)idx[1];
+                e.i3 = (uint8_t)idx[2];
+                e.row = (uint16_t)(s->out_off[c] / s->mul + k);
+                e.q = (uint16_t)(s->term_q0[t] + q);
+                e.coef = (float)v;
+                s->entries.push_back(e);
+            }
+    }
+    // grouped by output row (then weight, then position), the order the kernel sums in
+    std::stable_sort(s->entries.begin(), s->entries.end(), [](const tpc::SymcEntry &a, const tpc::SymcEntry &b) {
+        return a.row != b.row ? a.row < b.row : a.q < b.q;
+    });
+    return true;
+}
+}  // namespace
+
+namespace tpc {
+const SymcEntry *symc_table(const tp_symc *s, int *n) {
+    *n = (int)s->entries.size();
+    return s->entries.data();
+}
+int symc_mul(const tp_symc *s) { return s->mul; }
+int symc_D(const tp_symc *s) { return s->D; }
+int symc_rows_out(const tp_symc *s) { return s->dim_out / s->mul; }
+int symc_n_weights(const tp_symc *s) { return s->n_weights; }
+}  // namespace tpc

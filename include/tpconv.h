@@ -376,6 +376,52 @@ typedef struct {
 TPCONV_API tp_status tp_set_tuning(const tp_tuning *tuning);
 TPCONV_API tp_status tp_get_tuning(tp_tuning *tuning);
 
+/* Symmetric contraction (MACE-style; Lesson 12a, section 21.4.1: one line per
+ * body order nu, "[]·a[u]·b[u]·...·b[u] -> C[u]"; "cuEquivariance in PyTorch",
+ * Other operations and layers: uniform multiplicities, a contraction degree,
+ * a number of elements and integer element indices). Per node n and channel u,
+ * with b[n, i, u] the components of every input block of the node's features:
+ *   out[n, c, k, u] = sum_{nu=1..max_degree} sum_q a[element[n], q, u]
+ *                     * sum_{i_1..i_nu} B_q[i_1..i_nu, k] prod_t b[n, i_t, u]
+ * The basis tensors B_q of each (nu, output block) span the tensors symmetric
+ * in the nu slots and equivariant under rotations (and inversions for O(3));
+ * they are made canonical by the reduced row echelon form of the spanning set
+ * (flattened row-major over (i_1..i_nu, k)), each scaled to unit norm with a
+ * positive leading entry. For 32x0e+32x1o -> 32x0e and degrees 1..3 that is
+ * 1, 2 and 2 weights per channel with 1, 4 and 10 nonzero entries, as printed
+ * on the lesson. Weights are ordered term by term: degree ascending, then
+ * output block, then basis tensor. */
+typedef struct tp_symc tp_symc;
+typedef struct {
+    int32_t mul, dim_in, dim_out, max_degree;
+    int32_t n_weights;             /* per element and channel */
+    int32_t n_terms;               /* (degree, output block) pairs with a basis */
+    int32_t num_paths[3];          /* nonzero basis entries of degree 1, 2, 3 */
+    int32_t weights_per_degree[3];
+} tp_symc_info;
+/* irreps_in: input blocks of degrees <= 2, one multiplicity (a multiple of 32);
+ * irreps_out: output blocks of degrees <= 3, the same multiplicity; max_degree
+ * 1..3. TP_ERR_PARSE / TP_ERR_UNSUPPORTED / TP_ERR_ARG as tp_desc_create. */
+TPCONV_API tp_status tp_symc_create(const char *irreps_in, const char *irreps_out, int32_t max_degree,
+                                    tp_symc **out);
+TPCONV_API tp_status tp_symc_query(const tp_symc *symc, tp_symc_info *info);
+/* Term t: its degree, output block, number of basis tensors and (when basis
+ * is not NULL) the dense basis [n_q][D]..[D][2L+1] as float64 into host memory
+ * of `capacity` doubles. */
+TPCONV_API tp_status tp_symc_term(const tp_symc *symc, int32_t t, int32_t *nu, int32_t *out_block, int32_t *n_q,
+                                  double *basis, int64_t capacity);
+TPCONV_API void tp_symc_destroy(tp_symc *symc);
+/* x: device float32 [N][dim_in] (ir_mul), 16-byte aligned; weights: device
+ * float32 [num_elements][n_weights][mul], 8-byte aligned; element: device
+ * int32 [N] in [0, num_elements) (an index outside sets TP_DEV_ERR_INDEX and
+ * the node's row is zero); out: device float32 [N][dim_out] (ir_mul), 16-byte
+ * aligned, fully overwritten. Misaligned pointers give TP_ERR_ALIGN; a basis
+ * with more than 2000 nonzero entries or 512 (output row, weight) pairs gives
+ * TP_ERR_UNSUPPORTED. Asynchronous on `stream`; nothing is allocated. */
+TPCONV_API tp_status tp_symmetric_contraction(const tp_symc *symc, const float *x, const float *weights,
+                                              const int32_t *element, int32_t N, int32_t num_elements, float *out,
+                                              void *stream);
+
 /* Read (and, when reset != 0, clear) the current device's status word into
  * *flags (TP_DEV_ERR_* bits). Synchronises `stream`. */
 TPCONV_API tp_status tp_device_status(int32_t *flags, int32_t reset, void *stream);

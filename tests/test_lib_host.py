@@ -117,3 +117,34 @@ def test_tuning_hooks_validate_and_reset(tpc):
     assert tpc.tp_get_tuning()["ring_rounds"] == 4
     tpc.tp_set_tuning()
     assert tpc.tp_get_tuning() == {f: 0 for f in tpc.TUNING_FIELDS}
+
+
+SYMC_CASES = [("32x0e+32x1o", "32x0e", 3), ("32x0e+32x1o+32x2e", "32x0e+32x1o", 3), ("32x0+32x1", "32x0+32x1", 2),
+              ("32x1o", "32x0e+32x1o+32x2e", 3)]
+
+
+@pytest.mark.parametrize("case", SYMC_CASES, ids=lambda c: "|".join(map(str, c)))
+def test_symmetric_contraction_basis_matches_oracle(tpc, case):
+    """The library builds its basis from symmetrised Clebsch-Gordan coupling
+    trees; the oracle as a null space of the equivariance and symmetry
+    constraints. Both reduce to the same canonical form."""
+    from oracle import symc
+    irr_in, irr_out, deg = case
+    s = tpc.tp_symc_create(irr_in, irr_out, deg)
+    plan = symc.SymPlan(irr_in, irr_out, range(1, deg + 1))
+    assert s.n_terms == len(plan.terms) and s.n_weights == plan.n_weights
+    assert s.num_paths == [plan.num_paths(n) for n in range(1, deg + 1)]
+    assert (s.dim_in, s.dim_out) == (plan.dim_in, plan.dim_out)
+    for t, (nu, c, B) in enumerate(plan.terms):
+        assert tpc.tp_symc_term(s, t, plan.D)[:2] == (nu, c)
+        got = tpc.tp_symc_basis(s, t, plan.D, B.shape[-1])
+        np.testing.assert_allclose(got, B, atol=1e-12)
+
+
+def test_symmetric_contraction_lesson_counts(tpc):
+    import json
+    g = json.load(open(os.path.join(os.path.dirname(HEADER), "..", "tests", "golden",
+                                    "pages_worked_examples.json")))["symmetric_contraction_32x0e32x1o"]
+    s = tpc.tp_symc_create(g["irreps_in"], g["irreps_out"], max(g["degrees"]))
+    assert s.num_paths == g["num_paths"]
+    assert "+".join(f"{n * s.mul}x0e" for n in s.weights_per_degree) == g["weight_irreps"]
