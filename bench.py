@@ -239,10 +239,12 @@ def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 10
     dx = torch.empty((n, desc.dim_x), device=dev)
     dw = torch.empty((E, desc.weight_numel), device=dev)
     dsh = torch.empty((E, desc.dim_sh), device=dev)
+    nb = tpc.tp_conv_backward_workspace_size(desc, tpc.TP_F32, n, E)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
 
     def bwd():
         tpc.tp_conv_backward(desc, go, inp["x"], inp["sh"], inp["w"], inp["src"], dst, inp["row_ptr"], src_perm,
-                             src_row_ptr, dx=dx, dw=dw, dsh=dsh, stream=stream)
+                             src_row_ptr, dx=dx, dw=dw, dsh=dsh, workspace=ws, stream=stream)
 
     for _ in range(3):
         bwd()
@@ -258,7 +260,9 @@ def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 10
         raise RuntimeError("device status set during the backward timing")
     nbytes = backward_bytes(desc, n, E)
     return {"bwd_us": bwd_us, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (bwd_us * 1e-6) / 1e9,
-            "steps": steps, "kernels": "seg_conv_kernel (dw, dsh by destination; dx by source)"}
+            "steps": steps, "launches_per_call": 2,
+            "kernels": ("ring_bwd_kernel (one pass by source: dx, dw, dsh) + carry_fixup_kernel (partial dx rows)"
+                        if nb else "seg_conv_kernel (dw, dsh by destination; dx by source)")}
 
 
 _BUILT = {}

@@ -44,7 +44,7 @@ EXPORTS = ["tp_desc_create", "tp_desc_create_unsimplified", "tp_desc_query", "tp
            "tp_conv_forward_vec", "tp_conv_forward_mlp", "tp_conv_forward_ex_workspace_size", "tp_conv_forward_ex",
            "tp_transpose_layout", "tp_symc_create", "tp_symc_query", "tp_symc_term", "tp_symc_destroy",
            "tp_symmetric_contraction",
-           "tp_conv_backward", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
+           "tp_conv_backward", "tp_conv_backward_workspace_size", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
            "tp_abi_version"]
 
 
@@ -64,7 +64,9 @@ class _Info(ctypes.Structure):
 class _Tuning(ctypes.Structure):
     _fields_ = [("ring_stage_bytes", ctypes.c_int32), ("ring_stages", ctypes.c_int32), ("ring_warps", ctypes.c_int32),
                 ("ring_rounds", ctypes.c_int32), ("ring_pack", ctypes.c_int32), ("disable_split", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_int64), ("disable_mma", ctypes.c_int32), ("mma_stages", ctypes.c_int32)]
+                ("wait_limit_ns", ctypes.c_int64), ("disable_mma", ctypes.c_int32), ("mma_stages", ctypes.c_int32),
+                ("bwd_stage_bytes", ctypes.c_int32), ("bwd_stages", ctypes.c_int32), ("bwd_warps", ctypes.c_int32),
+                ("disable_ring_bwd", ctypes.c_int32)]
 
 
 class _Mlp(ctypes.Structure):
@@ -114,7 +116,9 @@ _sigs = {
     "tp_symc_query": [_vp, ctypes.POINTER(_SymcInfo)],
     "tp_symc_term": [_vp, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp, _i64],
     "tp_symmetric_contraction": [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp],
-    "tp_conv_backward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp],
+    "tp_conv_backward_workspace_size": [_vp, ctypes.c_int, _i32, _i64, ctypes.POINTER(_sz)],
+    "tp_conv_backward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp,
+                         _vp, _vp, _sz, _vp],
     "tp_device_status": [ctypes.POINTER(_i32), _i32, _vp],
     "tp_set_tuning": [ctypes.POINTER(_Tuning)],
     "tp_get_tuning": [ctypes.POINTER(_Tuning)],
@@ -495,11 +499,22 @@ def tp_transpose_layout(desc: Descriptor, which: str, source: str, src, dst=None
     return dst
 
 
+def tp_conv_backward_workspace_size(desc: Descriptor, dtype: int, n_src: int, E: int) -> int:
+    n = _sz()
+    _check(_lib.tp_conv_backward_workspace_size(desc.handle, dtype, n_src, E, ctypes.byref(n)),
+           "tp_conv_backward_workspace_size")
+    return int(n.value)
+
+
 def tp_conv_backward(desc: Descriptor, grad_out, x, sh, w, src, dst, row_ptr, src_perm, src_row_ptr,
-                     dx=None, dw=None, dsh=None, stream=None):
+                     dx=None, dw=None, dsh=None, workspace="auto", stream=None):
     """(dx, dw, dsh) float32 for destination-sorted edges; (src_perm,
-    src_row_ptr) is tp_csr_build(src, n_src) in that edge order."""
+    src_row_ptr) is tp_csr_build(src, n_src) in that edge order. x and w are
+    both float32 or both bfloat16 (float32 math); grad_out and sh float32.
+    `workspace`: a uint8 CUDA tensor of tp_conv_backward_workspace_size bytes,
+    "auto" to allocate one here, or None."""
     torch = _torch()
+    dtype = _fwd_dtype(x, w)
     E = src.shape[0]
     n_src, n_dst = x.shape[0], grad_out.shape[0]
     if dx is None:
@@ -508,15 +523,20 @@ def tp_conv_backward(desc: Descriptor, grad_out, x, sh, w, src, dst, row_ptr, sr
         dw = torch.empty((E, desc.weight_numel), dtype=torch.float32, device=x.device)
     if dsh is None:
         dsh = torch.empty((E, desc.dim_sh), dtype=torch.float32, device=x.device)
+    if isinstance(workspace, str):
+        nb = tp_conv_backward_workspace_size(desc, dtype, n_src, E)
+        workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_n = workspace.numel() if workspace is not None else 0
     f = torch.float32
-    _check(_lib.tp_conv_backward(desc.handle, _dev_ptr(grad_out, "grad_out", f, 2), _dev_ptr(x, "x", f, 2),
-                                 _dev_ptr(sh, "sh", f, 2), _dev_ptr(w, "w", f, 2),
+    _check(_lib.tp_conv_backward(desc.handle, dtype, _dev_ptr(grad_out, "grad_out", f, 2), _dev_ptr(x, "x", None, 2),
+                                 _dev_ptr(sh, "sh", f, 2), _dev_ptr(w, "w", None, 2),
                                  _dev_ptr(src, "src", torch.int32, 1), _dev_ptr(dst, "dst", torch.int32, 1),
                                  _dev_ptr(row_ptr, "row_ptr", torch.int32, 1),
                                  _dev_ptr(src_perm, "src_perm", torch.int32, 1),
                                  _dev_ptr(src_row_ptr, "src_row_ptr", torch.int32, 1), n_src, n_dst, E,
                                  _dev_ptr(dx, "dx", f, 2), _dev_ptr(dw, "dw", f, 2), _dev_ptr(dsh, "dsh", f, 2),
-                                 _stream(stream)),
+                                 ws_ptr, ws_n, _stream(stream)),
            "tp_conv_backward")
     return dx, dw, dsh
 

@@ -31,6 +31,12 @@ cudaError_t transpose_rows(const tp_desc *d, int which, int from, const void *sr
 cudaError_t scale_rows_by_inverse_degree(float *out, const int32_t *row_ptr, int32_t n, int32_t dim,
                                          cudaStream_t stream);
 size_t mma_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
+size_t ring_bwd_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
+cudaError_t ring_backward(const tp_desc *d, tp_dtype dtype, const float *grad_out, const void *x, const float *sh,
+                          const void *w, const int32_t *src, const int32_t *dst, const int32_t *src_perm,
+                          const int32_t *src_row_ptr, int32_t N_src, int32_t N_dst, int64_t E, float *dx, float *dw,
+                          float *dsh, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
+                          cudaStream_t stream);
 cudaError_t mma_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
                         const int32_t *src, const int32_t *row_ptr, int32_t N_src, int32_t N_dst, int64_t E,
                         float *out, void *ws, size_t ws_bytes, int dev, int sms, int smem_optin, int *status,
@@ -448,28 +454,56 @@ extern "C" tp_status tp_transpose_layout(const tp_desc *desc, int32_t which, tp_
                : TP_ERR_CUDA;
 }
 
-extern "C" tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out, const float *x, const float *sh,
-                                      const float *w, const int32_t *src, const int32_t *dst, const int32_t *row_ptr,
-                                      const int32_t *src_perm, const int32_t *src_row_ptr, int32_t N_src,
-                                      int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh, void *stream) {
+extern "C" tp_status tp_conv_backward_workspace_size(const tp_desc *desc, tp_dtype dtype, int32_t N_src, int64_t E,
+                                                     size_t *bytes) {
+    if (!desc || !bytes || N_src < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
+    DevInfo dev;
+    tp_status st = dev_info(dev);
+    if (st != TP_OK) return st;
+    *bytes = ring_bwd_workspace_bytes(desc, dtype, E, dev.dev, dev.sms, dev.smem_optin);
+    return TP_OK;
+}
+
+extern "C" tp_status tp_conv_backward(const tp_desc *desc, tp_dtype dtype, const float *grad_out, const void *x,
+                                      const float *sh, const void *w, const int32_t *src, const int32_t *dst,
+                                      const int32_t *row_ptr, const int32_t *src_perm, const int32_t *src_row_ptr,
+                                      int32_t N_src, int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
     if (!desc || N_src < 0 || N_dst < 0 || E < 0 || E >= (int64_t(1) << 31)) return TP_ERR_ARG;
+    if (dtype != TP_F32 && dtype != TP_BF16_IN_F32_OUT) return TP_ERR_ARG;
     if (desc->layout != TP_IR_MUL || desc->unsimp) return TP_ERR_UNSUPPORTED;
     if ((N_src > 0 && (!dx || !src_row_ptr)) || (N_dst > 0 && !row_ptr)) return TP_ERR_ARG;
     if (E > 0 && (!grad_out || !x || !sh || !w || !src || !dst || !src_perm || !dw || !dsh)) return TP_ERR_ARG;
     if (E > 0 && (N_src == 0 || N_dst == 0)) return TP_ERR_INDEX;
     const Tables &T = desc->tab;
-    if (((T.dim_x * 4) & 15) || ((T.wnum * 4) & 15) || ((T.dim_out * 4) & 15)) return TP_ERR_ALIGN;
+    const int esz = dtype == TP_F32 ? 4 : 2;
+    if (((T.dim_x * esz) & 15) || ((T.wnum * esz) & 15) || ((T.dim_out * 4) & 15) || ((T.wnum * 4) & 15))
+        return TP_ERR_ALIGN;
     if ((dx && !aligned16(dx)) ||
         (E > 0 && (!aligned16(grad_out) || !aligned16(x) || !aligned16(w) || !aligned16(dw) || !aligned4(sh) ||
-                   !aligned4(dsh))))
+                   !aligned4(dsh))) ||
+        (workspace && !aligned16(workspace)))
         return TP_ERR_ALIGN;
-    Shape shp;
-    if (!pick_shape(desc->lmax_in, desc->lmax_out, shp)) return TP_ERR_UNSUPPORTED;
-    const int cpt = pick_cpt(T.mul);
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N_src > 0) {
+        const cudaError_t e = ring_backward(desc, dtype, grad_out, x, sh, w, src, dst, src_perm, src_row_ptr, N_src,
+                                            N_dst, E, dx, dw, dsh, workspace, workspace_bytes, dev.dev, dev.sms,
+                                            dev.smem_optin, dev.status, s);
+        if (e == cudaSuccess) return TP_OK;
+        if (e != cudaErrorNotSupported) {
+            (void)cudaGetLastError();
+            return TP_ERR_CUDA;
+        }
+    }
+    // the generic two-kernel backward: float32, any descriptor the seg kernels cover
+    if (dtype != TP_F32) return TP_ERR_UNSUPPORTED;
+    Shape shp;
+    if (!pick_shape(desc->lmax_in, desc->lmax_out, shp)) return TP_ERR_UNSUPPORTED;
+    const int cpt = pick_cpt(T.mul);
     if (E > 0 && N_dst > 0) {  // dw, dsh: warp per destination
         const void *fn = seg_bwde_f32_kernel(shp, cpt);
         if (!fn) return TP_ERR_UNSUPPORTED;
@@ -531,7 +565,10 @@ extern "C" tp_status tp_set_tuning(const tp_tuning *t) {
                         (v.ring_rounds == 0 || (v.ring_rounds >= 1 && v.ring_rounds <= kRingMaxPiecesPerWarp)) &&
                         v.ring_pack >= 0 && v.ring_pack <= 2 && (v.disable_split == 0 || v.disable_split == 1) &&
                         v.wait_limit_ns >= 0 && (v.disable_mma == 0 || v.disable_mma == 1) &&
-                        (v.mma_stages == 0 || (v.mma_stages >= 3 && v.mma_stages <= 8));
+                        (v.mma_stages == 0 || (v.mma_stages >= 3 && v.mma_stages <= 8)) &&
+                        v.bwd_stage_bytes >= 0 && (v.bwd_stages == 0 || (v.bwd_stages >= 2 && v.bwd_stages <= 8)) &&
+                        (v.bwd_warps == 0 || (v.bwd_warps >= 1 && v.bwd_warps <= kRingMaxWarps)) &&
+                        (v.disable_ring_bwd == 0 || v.disable_ring_bwd == 1);
         if (!ok) return TP_ERR_ARG;
     }
     std::lock_guard<std::mutex> lk(g_tune_mu);

@@ -51,6 +51,25 @@ constexpr bool m_entry_possible(int la, int lb, int lc, int i, int k) {
     return false;
 }
 
+// The harmonic components j (0..2lb, ascending) that can couple input row i
+// to output row k of path (la, lb, lc) under the same rule: at most two, one
+// per value of |m2|; `slot` 0 or 1, -1 when there is no such component.
+constexpr int m_entry_j(int la, int lb, int lc, int i, int k, int slot) {
+    const int m1 = i - la, m3 = k - lc;
+    const bool odd = ((la + lb + lc) & 1) != 0;
+    int found = 0;
+    for (int m2 = -lb; m2 <= lb; ++m2) {
+        const int a = pabs(m1), b = pabs(m2), c = pabs(m3);
+        if (!(c == a + b || c == pabs(a - b))) continue;
+        bool sin_prod = (m1 < 0) != (m2 < 0);
+        if (odd) sin_prod = !sin_prod;
+        if (sin_prod != (m3 < 0)) continue;
+        if (found == slot) return m2 + lb;
+        ++found;
+    }
+    return -1;
+}
+
 constexpr Program make_natural_program(int LI, int LSH, int LO) {
     Program P{};
     P.n = 0;

@@ -153,9 +153,11 @@ std::map<PlanKey, std::unique_ptr<RingLaunch>> g_plans;  // nullptr: no ring ker
 }  // namespace
 
 void mma_cache_forget(uint64_t uid);
+void bwd_cache_forget(uint64_t uid);
 
 void launch_cache_forget(uint64_t uid) {
     mma_cache_forget(uid);
+    bwd_cache_forget(uid);
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (auto it = g_plans.begin(); it != g_plans.end();) it = it->first.uid == uid ? g_plans.erase(it) : std::next(it);
 }

@@ -328,22 +328,35 @@ TPCONV_API tp_status tp_conv_forward_ex(const tp_desc *desc, const tp_forward_ar
 TPCONV_API tp_status tp_transpose_layout(const tp_desc *desc, int32_t which, tp_layout from, const void *src,
                                          void *dst, int64_t rows, int32_t elem_bytes, void *stream);
 
-/* Backward pass of tp_conv_forward (float32), the exact gradients of
- * <grad_out, out> with respect to x, w and sh ("cuEquivariance in PyTorch",
- * CPU tensor product and backward: gradients with respect to both inputs and
- * the weights; the forward is linear in each of them, so these sums are exact):
+/* Backward pass of tp_conv_forward, the exact gradients of <grad_out, out>
+ * with respect to x, w and sh ("cuEquivariance in PyTorch", CPU tensor
+ * product and backward: gradients with respect to both inputs and the
+ * weights; the forward is linear in each of them, so these sums are exact):
  *   dx[s,a,i,u] = sum_{e: src[e]=s} sum_{p: a_p=a} w[e,p,u] sum_{j,k} C_p[i,j,k] sh[e,b,j] g[dst[e],c,k,u]
  *   dw[e,p,u]   = sum_{i,j,k} C_p[i,j,k] x[src[e],a,i,u] sh[e,b,j] g[dst[e],c,k,u]
  *   dsh[e,b,j]  = sum_{p: b_p=b} sum_{i,k,u} C_p[i,j,k] x[src[e],a,i,u] w[e,p,u] g[dst[e],c,k,u]
+ * dtype TP_F32: x and w float32; TP_BF16_IN_F32_OUT: x and w bfloat16 (the
+ * forward's bfloat16 inputs), every product and sum in float32. grad_out
+ * [N_dst][dim_out], sh [E][dim_sh] and all three gradients are float32.
  * Edges are in destination-sorted order (row_ptr as for the forward; dst[E]
  * the sorted destination of each edge). The source CSR (src_perm, src_row_ptr)
  * is tp_csr_build of `src` in that same edge order: src_perm lists edge
  * positions grouped by source. dx [N_src][dim_x], dw [E][weight_numel] and
- * dsh [E][dim_sh] are fully overwritten. Deterministic (no atomics). */
-TPCONV_API tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out, const float *x, const float *sh,
-                           const float *w, const int32_t *src, const int32_t *dst, const int32_t *row_ptr,
-                           const int32_t *src_perm, const int32_t *src_row_ptr, int32_t N_src,
-                           int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh, void *stream);
+ * dsh [E][dim_sh] are fully overwritten (for every edge src_perm lists; an
+ * edge whose destination is out of range gets zero dw and dsh rows and sets
+ * TP_DEV_ERR_INDEX). Deterministic (no atomics).
+ * workspace: device memory of tp_conv_backward_workspace_size bytes (16-byte
+ * aligned) for the partial dx rows of sources whose edges two warps share;
+ * with a smaller (or NULL) workspace the call uses fewer warps, or the
+ * generic two-kernel backward (float32 only). TP_ERR_UNSUPPORTED for
+ * bfloat16 inputs when the descriptor has no compiled path program. */
+TPCONV_API tp_status tp_conv_backward_workspace_size(const tp_desc *desc, tp_dtype dtype, int32_t N_src, int64_t E,
+                                                     size_t *bytes);
+TPCONV_API tp_status tp_conv_backward(const tp_desc *desc, tp_dtype dtype, const float *grad_out, const void *x,
+                                      const float *sh, const void *w, const int32_t *src, const int32_t *dst,
+                                      const int32_t *row_ptr, const int32_t *src_perm, const int32_t *src_row_ptr,
+                                      int32_t N_src, int32_t N_dst, int64_t E, float *dx, float *dw, float *dsh,
+                                      void *workspace, size_t workspace_bytes, void *stream);
 
 /* Launch tuning and test hooks. The pages have no counterpart: these settings
  * exist for tests and tuning sweeps, and normal use never needs them. They
@@ -361,6 +374,10 @@ TPCONV_API tp_status tp_conv_backward(const tp_desc *desc, const float *grad_out
  *                     keep the 1 s limit.
  *   disable_mma       1: bfloat16 inputs skip the tensor-core kernel
  *   mma_stages        shared-memory stages of the tensor-core kernel, 3..8
+ *   bwd_stage_bytes   target bytes per chunk of the backward's warp ring (>= 0)
+ *   bwd_stages        stages per backward warp ring, 2..8
+ *   bwd_warps         warps per block of the backward ring kernel, 1..8
+ *   disable_ring_bwd  1: float32 backward uses the generic two-kernel path
  * tp_set_tuning(NULL) restores every default. TP_ERR_ARG for a field out of range. */
 typedef struct {
     int32_t ring_stage_bytes;
@@ -372,6 +389,10 @@ typedef struct {
     int64_t wait_limit_ns;
     int32_t disable_mma;
     int32_t mma_stages;
+    int32_t bwd_stage_bytes;
+    int32_t bwd_stages;
+    int32_t bwd_warps;
+    int32_t disable_ring_bwd;
 } tp_tuning;
 TPCONV_API tp_status tp_set_tuning(const tp_tuning *tuning);
 TPCONV_API tp_status tp_get_tuning(tp_tuning *tuning);
