@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU-oracle sample time")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-backward", action="store_true", help="skip the backward timing (medium graph)")
+    ap.add_argument("--backward-steps", type=int, default=100, help="timed calls of the backward")
+    ap.add_argument("--no-symc", action="store_true", help="skip the symmetric contraction timing")
     return ap.parse_args()
 
 
@@ -91,24 +93,27 @@ def measured_sm_mhz() -> float:
     return 2070.0
 
 
-def source_hash() -> str:
+def source_hash(files) -> str:
+    """Hash of the kernel sources a traffic figure was taken on (paths relative
+    to the repository root)."""
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "equivariant_gnn_tensor_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files):
         h.update(f.encode())
-        h.update(open(os.path.join(d, f), "rb").read())
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel_key: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of that kernel (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     e = d.get(kernel_key)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or not all(os.path.exists(os.path.join(ROOT, f)) for f in e.get("files", [])):
+        return None
+    if not e.get("files") or e.get("source_hash") != source_hash(e["files"]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -606,12 +611,18 @@ def bench_ours(args):
             del g
             torch.cuda.empty_cache()
         line["configs"] = cfgs
-        line["symmetric_contraction"] = symmetric_contraction_bench(tpc, torch, device, stream, peak, peak_src, local)
+        if not args.no_symc:
+            line["symmetric_contraction"] = symmetric_contraction_bench(tpc, torch, device, stream, peak, peak_src,
+                                                                        local)
         if not args.no_backward:
             # the fwd+bwd workload: the medium graph and features with its own grad_out
             b = Forward("fwdbwd", args.seed, tpc, torch, device, stream)
-            bk = time_backward(tpc, torch, b.desc, b.inp, b.n, b.E, b.host[5], stream)
+            bk = time_backward(tpc, torch, b.desc, b.inp, b.n, b.E, b.host[5], stream, steps=args.backward_steps)
             bk["frac"] = bk["achieved_gbs"] / peak
+            bk["roofline"] = {"bound": "hbm", "achieved": bk["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                              "frac": bk["achieved_gbs"] / peak, "traffic": profiled_traffic("bwd:fwdbwd"),
+                              "algorithmic_bytes": bk["algorithmic_bytes"], "kernel_us": bk["bwd_us"],
+                              "peak_source": peak_src}
             bk["workload"] = b.describe()
             line["backward"] = bk
             del b
