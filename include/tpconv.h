@@ -187,8 +187,8 @@ TPCONV_API tp_status tp_csr_build(const int32_t *keys, int64_t E, int32_t N, int
  * passes keys and the outputs. E may be at most
  * tp_csr_build_noalloc_max_edges() (262144); larger E returns TP_ERR_CAPACITY
  * without launching anything. The first call on each device looks up the
- * array's device address (a one-time set-up, no allocation); make that first
- * call before any stream capture begins. All calls share the one array, so
+ * array's device address with a runtime query (a one-time set-up, no
+ * allocation). All calls share the one array, so
  * calls that overlap on the GPU (different streams, or different host
  * threads) race and must be serialised by the caller. Nothing in the array
  * needs to start at zero: every call overwrites what it reads. */
