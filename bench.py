@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward timing (medium graph)")
     ap.add_argument("--backward-steps", type=int, default=100, help="timed calls of the backward")
     ap.add_argument("--no-symc", action="store_true", help="skip the symmetric contraction timing")
+    ap.add_argument("--nodes", type=int, default=None,
+                    help="node count of the headline workload (same graph recipe; for profiling small cases)")
     return ap.parse_args()
 
 
@@ -172,12 +174,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+NODES_OVERRIDE = {}  # workload -> node count (--nodes)
+
+
 def build_inputs(wname: str, seed: int, tpc, torch, device):
     """Synthetic inputs of a workload, resident on `device`. Returns (wl, desc,
     inputs, n, E, host) with host = (x, w, src, dst, vec, grad_out) as drawn
     (grad_out None unless the workload has a backward)."""
+    import dataclasses
     from workloads import WORKLOADS, make_features, make_graph
     wl = WORKLOADS[wname]
+    if wname in NODES_OVERRIDE:   # the same graph recipe on fewer (or more) nodes, for profiling
+        wl = dataclasses.replace(wl, n_nodes=NODES_OVERRIDE[wname])
     desc = tpc.tp_desc_create(wl.irreps_in, wl.irreps_sh, wl.irreps_out)
     rng, src, dst, vec, n = make_graph(wl, seed)
     E = len(src)
@@ -440,7 +448,9 @@ def symmetric_contraction_bench(tpc, torch, device, stream, peak, peak_src, loca
             "value": N / (us * 1e-6), "unit": "nodes/s", "steps": steps, "kernel_us": us,
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                          "traffic": None, "algorithmic_bytes": nbytes, "kernel_us": us, "peak_source": peak_src},
-            "clocks": clk, "gpu_launches": steps}
+            "clocks": clk, "gpu_launches": steps,
+            "kernel": "symc_jit (compiled at run time for this descriptor; the table kernel symc_kernel when "
+                      "tp_set_tuning(disable_symc_jit=1))"}
 
 
 def tiny_latency(tpc, torch, device, stream, calls: int = 20000):
@@ -549,6 +559,8 @@ DEFAULT_STEPS = {"tiny": 20000, "medium": 2000, "large": 300, "xlarge": 500}
 
 
 def bench_ours(args):
+    if args.nodes:
+        NODES_OVERRIDE[args.workload] = args.nodes
     import torch
     world, rank, local = dist_env()
     if world > 1:

@@ -43,7 +43,7 @@ EXPORTS = ["tp_desc_create", "tp_desc_create_unsimplified", "tp_desc_query", "tp
            "tp_csr_build_noalloc_max_edges", "tp_conv_forward_workspace_size", "tp_conv_forward",
            "tp_conv_forward_vec", "tp_conv_forward_mlp", "tp_conv_forward_ex_workspace_size", "tp_conv_forward_ex",
            "tp_transpose_layout", "tp_symc_create", "tp_symc_query", "tp_symc_term", "tp_symc_destroy",
-           "tp_symmetric_contraction",
+           "tp_symmetric_contraction", "tp_symc_kernel_source",
            "tp_conv_backward", "tp_conv_backward_workspace_size", "tp_set_tuning", "tp_get_tuning", "tp_device_status", "tp_status_string",
            "tp_abi_version"]
 
@@ -66,7 +66,7 @@ class _Tuning(ctypes.Structure):
                 ("ring_rounds", ctypes.c_int32), ("ring_pack", ctypes.c_int32), ("disable_split", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64), ("disable_mma", ctypes.c_int32), ("mma_stages", ctypes.c_int32),
                 ("bwd_stage_bytes", ctypes.c_int32), ("bwd_stages", ctypes.c_int32), ("bwd_warps", ctypes.c_int32),
-                ("disable_ring_bwd", ctypes.c_int32)]
+                ("disable_ring_bwd", ctypes.c_int32), ("disable_symc_jit", ctypes.c_int32)]
 
 
 class _Mlp(ctypes.Structure):
@@ -116,6 +116,7 @@ _sigs = {
     "tp_symc_query": [_vp, ctypes.POINTER(_SymcInfo)],
     "tp_symc_term": [_vp, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp, _i64],
     "tp_symmetric_contraction": [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp],
+    "tp_symc_kernel_source": [_vp, _vp, _i64, ctypes.POINTER(_i64)],
     "tp_conv_backward_workspace_size": [_vp, ctypes.c_int, _i32, _i64, ctypes.POINTER(_sz)],
     "tp_conv_backward": [_vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _vp, _vp,
                          _vp, _vp, _sz, _vp],
@@ -219,6 +220,15 @@ def tp_symc_basis(symc: SymcDescriptor, t: int, D: int, K: int) -> np.ndarray:
     _check(_lib.tp_symc_term(symc.handle, t, ctypes.byref(_i32()), ctypes.byref(_i32()), ctypes.byref(_i32()),
                              arr.ctypes.data_as(_vp), arr.size), "tp_symc_term")
     return arr
+
+
+def tp_symc_kernel_source(symc: SymcDescriptor) -> str:
+    """The CUDA source of the kernel specialised for this descriptor."""
+    n = _i64()
+    _check(_lib.tp_symc_kernel_source(symc.handle, None, 0, ctypes.byref(n)), "tp_symc_kernel_source")
+    buf = ctypes.create_string_buffer(n.value + 1)
+    _check(_lib.tp_symc_kernel_source(symc.handle, buf, n.value + 1, ctypes.byref(n)), "tp_symc_kernel_source")
+    return buf.value.decode()
 
 
 def tp_symc_destroy(symc: SymcDescriptor):

@@ -19,7 +19,7 @@ LIB = os.path.join(HERE, "libtpconv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fvisibility=hidden"] + ARCH
-SOURCES = ["api.cu", "csr.cu", "sh.cu", "variants.cu", "unsimp.cu", "symc.cu", "ring_host.cu", "mma_host.cu", "ring_f32.cu", "ring_bf16.cu", "ring_vec_f32.cu", "ring_vec_bf16.cu", "ring_mlp_f32.cu", "ring_bwd_host.cu", "ring_bwd_f32.cu", "ring_bwd_bf16.cu", "seg_fwd_f32.cu", "seg_fwd_bf16.cu", "seg_bwdx_f32.cu",
+SOURCES = ["api.cu", "csr.cu", "sh.cu", "variants.cu", "unsimp.cu", "symc.cu", "symc_jit.cpp", "ring_host.cu", "mma_host.cu", "ring_f32.cu", "ring_bf16.cu", "ring_vec_f32.cu", "ring_vec_bf16.cu", "ring_mlp_f32.cu", "ring_bwd_host.cu", "ring_bwd_f32.cu", "ring_bwd_bf16.cu", "seg_fwd_f32.cu", "seg_fwd_bf16.cu", "seg_bwdx_f32.cu",
            "seg_bwde_f32.cu", "descriptor.cpp"]
 
 

@@ -21,6 +21,8 @@ int64_t csr_noalloc_max_edges();
 cudaError_t csr_noalloc_scratch(void **ptr);
 size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int dev, int sms, int smem_optin);
 cudaError_t indices_to_i32(const int64_t *in, int64_t n, int32_t *out, cudaStream_t stream);
+cudaError_t symc_jit_launch(const tp_symc *s, const float *x, const float *weights, const int32_t *element, int32_t N,
+                            int32_t num_elements, float *out, int dev, int sms, int *status, cudaStream_t stream);
 cudaError_t symc_launch(const tp_symc *s, const float *x, const float *weights, const int32_t *element, int32_t N,
                         int32_t num_elements, float *out, int sms, int smem_optin, int *status, cudaStream_t stream);
 cudaError_t unsimp_forward(const tp_desc *d, tp_dtype dtype, const void *x, const float *sh, const void *w,
@@ -568,7 +570,8 @@ extern "C" tp_status tp_set_tuning(const tp_tuning *t) {
                         (v.mma_stages == 0 || (v.mma_stages >= 3 && v.mma_stages <= 8)) &&
                         v.bwd_stage_bytes >= 0 && (v.bwd_stages == 0 || (v.bwd_stages >= 2 && v.bwd_stages <= 8)) &&
                         (v.bwd_warps == 0 || (v.bwd_warps >= 1 && v.bwd_warps <= kRingMaxWarps)) &&
-                        (v.disable_ring_bwd == 0 || v.disable_ring_bwd == 1);
+                        (v.disable_ring_bwd == 0 || v.disable_ring_bwd == 1) &&
+                        (v.disable_symc_jit == 0 || v.disable_symc_jit == 1);
         if (!ok) return TP_ERR_ARG;
     }
     std::lock_guard<std::mutex> lk(g_tune_mu);
@@ -594,8 +597,12 @@ extern "C" tp_status tp_symmetric_contraction(const tp_symc *symc, const float *
     DevInfo dev;
     tp_status st = dev_info(dev);
     if (st != TP_OK) return st;
-    const cudaError_t e = symc_launch(symc, x, weights, element, N, num_elements, out, dev.sms, dev.smem_optin,
-                                      dev.status, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorNotSupported;
+    if (!tuning_snapshot().t.disable_symc_jit)  // the kernel specialised for this descriptor
+        e = symc_jit_launch(symc, x, weights, element, N, num_elements, out, dev.dev, dev.sms, dev.status, s);
+    if (e == cudaErrorNotSupported)  // the table kernel
+        e = symc_launch(symc, x, weights, element, N, num_elements, out, dev.sms, dev.smem_optin, dev.status, s);
     if (e == cudaSuccess) return TP_OK;
     (void)cudaGetLastError();
     return e == cudaErrorNotSupported ? TP_ERR_UNSUPPORTED : TP_ERR_CUDA;

@@ -378,6 +378,8 @@ TPCONV_API tp_status tp_conv_backward(const tp_desc *desc, tp_dtype dtype, const
  *   bwd_stages        stages per backward warp ring, 2..8
  *   bwd_warps         warps per block of the backward ring kernel, 1..8
  *   disable_ring_bwd  1: float32 backward uses the generic two-kernel path
+ *   disable_symc_jit  1: the symmetric contraction uses its table kernel
+ *                     instead of the kernel compiled for the descriptor
  * tp_set_tuning(NULL) restores every default. TP_ERR_ARG for a field out of range. */
 typedef struct {
     int32_t ring_stage_bytes;
@@ -393,6 +395,7 @@ typedef struct {
     int32_t bwd_stages;
     int32_t bwd_warps;
     int32_t disable_ring_bwd;
+    int32_t disable_symc_jit;
 } tp_tuning;
 TPCONV_API tp_status tp_set_tuning(const tp_tuning *tuning);
 TPCONV_API tp_status tp_get_tuning(tp_tuning *tuning);
@@ -432,6 +435,12 @@ TPCONV_API tp_status tp_symc_query(const tp_symc *symc, tp_symc_info *info);
 TPCONV_API tp_status tp_symc_term(const tp_symc *symc, int32_t t, int32_t *nu, int32_t *out_block, int32_t *n_q,
                                   double *basis, int64_t capacity);
 TPCONV_API void tp_symc_destroy(tp_symc *symc);
+/* The CUDA source of the kernel tp_symmetric_contraction compiles for this
+ * descriptor (at run time, with NVRTC, once per device): the basis as
+ * straight-line code. Writes up to `capacity` bytes (NUL-terminated when it
+ * fits) into host memory `buf` and the full length (without the NUL) into
+ * *length. For inspection and tests; needs no GPU. */
+TPCONV_API tp_status tp_symc_kernel_source(const tp_symc *symc, char *buf, int64_t capacity, int64_t *length);
 /* x: device float32 [N][dim_in] (ir_mul), 16-byte aligned; weights: device
  * float32 [num_elements][n_weights][mul], 8-byte aligned; element: device
  * int32 [N] in [0, num_elements) (an index outside sets TP_DEV_ERR_INDEX and

@@ -111,7 +111,7 @@ def test_tuning_hooks_validate_and_reset(tpc):
     for bad in (dict(ring_stages=1), dict(ring_stages=9), dict(ring_warps=9), dict(ring_rounds=17),
                 dict(ring_pack=3), dict(disable_split=2), dict(wait_limit_ns=-1), dict(ring_stage_bytes=-4),
                 dict(disable_mma=2), dict(mma_stages=2), dict(mma_stages=9), dict(bwd_stage_bytes=-1),
-                dict(bwd_stages=1), dict(bwd_stages=9), dict(bwd_warps=9), dict(disable_ring_bwd=2)):
+                dict(bwd_stages=1), dict(bwd_stages=9), dict(bwd_warps=9), dict(disable_ring_bwd=2), dict(disable_symc_jit=2)):
         with pytest.raises(tpc.TPError) as ei:
             tpc.tp_set_tuning(**bad)
         assert tpc.STATUS_NAMES[ei.value.status] == "TP_ERR_ARG"
