@@ -235,24 +235,28 @@ def algorithmic_bytes(desc, n, E, esz, from_vectors=False, radial=False):
     return (w_bytes + E * per_edge_h + E * 4 + n * desc.dim_x * esz + n * desc.dim_out * 4 + (n + 1) * 4)
 
 
-def backward_bytes(desc, n, E):
-    """Compulsory bytes of one fp32 backward: w read and dw written, sh read and
-    dsh written, src and the source permutation, x and grad_out read, dx
-    written, both row-pointer arrays."""
-    return (2 * E * desc.weight_numel * 4 + 2 * E * desc.dim_sh * 4 + 2 * E * 4 + 3 * n * desc.dim_x * 4
-            + 2 * (n + 1) * 4)
+def backward_bytes(desc, n, E, esz=4):
+    """Compulsory bytes of one backward: w read (esz bytes an element) and dw
+    written (float32), sh read and dsh written, src and the source
+    permutation, x read (esz), grad_out read, dx written, both row-pointer
+    arrays."""
+    return (E * desc.weight_numel * (esz + 4) + 2 * E * desc.dim_sh * 4 + 2 * E * 4
+            + n * desc.dim_x * (esz + 4) + n * desc.dim_out * 4 + 2 * (n + 1) * 4)
 
 
-def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 100):
+def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 100, bf16: bool = False):
     """Backward (dx, dw, dsh) of the medium graph with its own grad_out, the
     fwd+bwd configuration's second half: CUDA events over `steps` calls;
-    returns the dict reported under "backward"."""
+    returns the dict reported under "backward". With bf16, x and w are the
+    same values rounded to bfloat16 (the gradients stay float32)."""
     go, dst, src_perm, src_row_ptr = backward_inputs(tpc, torch, inp, n, grad_out)
     dev = inp["x"].device
+    if bf16:
+        inp = dict(inp, x=inp["x"].to(torch.bfloat16), w=inp["w"].to(torch.bfloat16))
     dx = torch.empty((n, desc.dim_x), device=dev)
     dw = torch.empty((E, desc.weight_numel), device=dev)
     dsh = torch.empty((E, desc.dim_sh), device=dev)
-    nb = tpc.tp_conv_backward_workspace_size(desc, tpc.TP_F32, n, E)
+    nb = tpc.tp_conv_backward_workspace_size(desc, tpc.TP_BF16_IN_F32_OUT if bf16 else tpc.TP_F32, n, E)
     ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
 
     def bwd():
@@ -271,7 +275,7 @@ def time_backward(tpc, torch, desc, inp, n, E, grad_out, stream, steps: int = 10
     bwd_us = e0.elapsed_time(e1) / steps * 1e3
     if tpc.tp_device_status(reset=True) != 0:
         raise RuntimeError("device status set during the backward timing")
-    nbytes = backward_bytes(desc, n, E)
+    nbytes = backward_bytes(desc, n, E, 2 if bf16 else 4)
     return {"bwd_us": bwd_us, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (bwd_us * 1e-6) / 1e9,
             "steps": steps, "launches_per_call": 2,
             "kernels": ("ring_bwd_kernel (one pass by source: dx, dw, dsh) + carry_fixup_kernel (partial dx rows)"
@@ -637,6 +641,11 @@ def bench_ours(args):
                               "peak_source": peak_src}
             bk["workload"] = b.describe()
             line["backward"] = bk
+            bh = time_backward(tpc, torch, b.desc, b.inp, b.n, b.E, b.host[5], stream, steps=args.backward_steps,
+                               bf16=True)
+            bh["frac"] = bh["achieved_gbs"] / peak
+            bh["workload"] = b.describe() + ", x and w rounded to bf16 (gradients fp32)"
+            line["backward_bf16"] = bh
             del b
             torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
