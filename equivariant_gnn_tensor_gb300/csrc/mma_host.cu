@@ -155,10 +155,12 @@ size_t carry_bytes(int pieces, int dim_out) {
     return (a + 255) / 256 * 256 + (size_t)2 * pieces * sizeof(int32_t);
 }
 
-// CTAs for E edges: two per SM, but at least ~256 edges per CTA.
+// CTAs for E edges: two per SM, but at least ~32 edges per CTA (a CTA walks
+// its edge pairs one stage after another; on a small graph more CTAs keep more
+// of them in flight).
 int mma_ctas(const MmaPlan &pl, int64_t E, int sms) {
     long long c = (long long)sms * pl.occ;
-    const long long by_edges = (E + 255) / 256;
+    const long long by_edges = (E + 31) / 32;
     if (c > by_edges) c = by_edges;
     return c < 1 ? 1 : (int)c;
 }

@@ -146,10 +146,11 @@ const BwdLaunch *cached_bwd_plan(const tp_desc *d, tp_dtype dtype, int dev, int 
     return p;
 }
 
-// every resident warp slot, but at least ~32 edges per warp
+// every resident warp slot, but at least ~4 edges per warp (on a small graph
+// more warps keep more chunks in flight at once)
 void bwd_geometry(const BwdLaunch &bl, int64_t E, int sms, int &n_warps) {
     long long nw = (long long)sms * bl.occ * bl.wpb;
-    const long long by_edges = (E + 31) / 32;
+    const long long by_edges = (E + 3) / 4;
     if (nw > by_edges) nw = by_edges;
     if (nw < 1) nw = 1;
     n_warps = (int)nw;

@@ -174,11 +174,13 @@ static const RingLaunch *cached_plan(const tp_desc *d, tp_dtype dtype, int dev, 
     return p;
 }
 
-// Warps and pieces for E edges: every resident warp slot, but at least ~64
-// edges per warp.
+// Warps and pieces for E edges: every resident warp slot, but at least ~8
+// edges (one or two chunks) per warp. A warp walks its chunks one ring stage
+// after another, so on a small graph spreading the edges over more warps keeps
+// every chunk in flight at once instead of paying one copy latency per chunk.
 static void ring_geometry(const RingLaunch &rl, int64_t E, int sms, int &n_warps, int &n_pieces) {
     long long nw = (long long)sms * rl.occ * rl.wpb;
-    const long long by_edges = (E + 63) / 64;
+    const long long by_edges = (E + 7) / 8;
     if (nw > by_edges) nw = by_edges;
     if (nw < 1) nw = 1;
     n_warps = (int)nw;

@@ -65,20 +65,26 @@ def test_fullsize_sampled_rows(tpc, name):
             assert not np.any(g)
 
 
-def test_backward_fwdbwd_fullsize(tpc):
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_backward_fwdbwd_fullsize(tpc, bf16):
     """The backward of the fwd+bwd configuration at its full size (the medium
     graph, N=4096, E=131064, 13 paths, mul 128, with its own grad_out), run
-    exactly as bench.py times it, checked on samples the fp64 C oracle
-    recomputes from the host copies: about 50 dx rows (random ones, the first,
-    the last and the source with the most edges) through the oracle's own
-    source CSR, and about 2000 edges of dw and dsh."""
+    exactly as bench.py times it (float32 x and w, and the same values rounded
+    to bfloat16), checked on samples the fp64 C oracle recomputes from the host
+    copies: about 50 dx rows (random ones, the first, the last and the source
+    with the most edges) through the oracle's own source CSR, and about 2000
+    edges of dw and dsh."""
     import bench
     dev = torch.device("cuda:0")
     wl, desc, inp, n, E, host = bench.build_inputs("fwdbwd", 0, tpc, torch, dev)
     x, w, src, dst, vec, g = host
     go, dst_d, sp, srp = bench.backward_inputs(tpc, torch, inp, n, g)
-    dx, dw, dsh = tpc.tp_conv_backward(desc, go, inp["x"], inp["sh"], inp["w"], inp["src"], dst_d, inp["row_ptr"],
-                                       sp, srp)
+    xd, wd = inp["x"], inp["w"]
+    if bf16:
+        xd, wd = xd.to(torch.bfloat16), wd.to(torch.bfloat16)
+        x = torch.as_tensor(x).to(torch.bfloat16).float().numpy()
+        w = torch.as_tensor(w).to(torch.bfloat16).float().numpy()
+    dx, dw, dsh = tpc.tp_conv_backward(desc, go, xd, inp["sh"], wd, inp["src"], dst_d, inp["row_ptr"], sp, srp)
     torch.cuda.synchronize()
     assert tpc.tp_device_status(reset=True) == 0
 
