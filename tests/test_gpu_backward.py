@@ -242,11 +242,11 @@ def test_ring_backward_wait_timeout_is_reported_and_writes_stay_in_bounds(tpc):
     waits after a failure keep the full limit), the call returns,
     TP_DEV_ERR_TIMEOUT is reported, nothing outside dx, dw and dsh changes
     (guard rows around each keep their sentinel), and the next call with the
-    default settings is correct again. One-edge chunks of the 32-channel
-    shape (little arithmetic per chunk) let a warp reach chunks still in
-    flight."""
-    n, E = 4000, 200000
-    prob = make_problem(*SHAPES[1], n_src=n, n_dst=n, E=E, seed=80)
+    default settings is correct again. One-edge chunks of the smallest
+    program shape (little arithmetic per chunk) let a warp reach chunks still
+    in flight."""
+    n, E = 4000, 400000
+    prob = make_problem(*(t.format(m=32) for t in PROGRAM_SHAPES[0]), n_src=n, n_dst=n, E=E, seed=80)
     g_np = np.random.default_rng(81).standard_normal((n, prob["plan"].dim_out))
     desc = tpc.tp_desc_create(*prob["irreps"])
     g = gpu_sorted_inputs(tpc, prob)
@@ -262,7 +262,7 @@ def test_ring_backward_wait_timeout_is_reported_and_writes_stay_in_bounds(tpc):
     bw, dw = banded(E, desc.weight_numel)
     bs, dsh = banded(E, desc.dim_sh)
     hit = False
-    for _ in range(5):
+    for _ in range(10):
         with tuning(tpc, wait_limit_ns=1, bwd_stage_bytes=1):
             tpc.tp_conv_backward(desc, go, g["x"], g["sh"], g["w"], g["src"], g["dst"], g["row_ptr"], sp, srp,
                                  dx=dx, dw=dw, dsh=dsh)
