@@ -107,7 +107,8 @@ def source_hash(files) -> str:
 
 def profiled_traffic(kernel_key: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current sources of that kernel (else None)."""
+    the current device code of that kernel (the files listed with it: kernel
+    source, shared headers, instantiation file), else None."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
