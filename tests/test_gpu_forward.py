@@ -88,7 +88,7 @@ def test_degree_extremes_and_empty_rows(tpc, workspace):
     prob = make_problem(*SHAPES[1], n_src=50, n_dst=n_dst, E=len(dst), seed=6, dst=dst)
     out, _, _ = run(tpc, prob, workspace=workspace)
     ref = oracle_forward(prob)
-    # destination 3 sums 1000 edges: judge every row against its own RMS (the
+    # destination 3 sums 1000 edges: measure every row against its own RMS (the
     # whole-tensor RMS, diluted by empty rows, understates its magnitude)
     on = out.double().cpu().numpy()
     for d, c in zip(*np.unique(dst, return_counts=True)):
