@@ -281,3 +281,20 @@ def test_ring_backward_wait_timeout_is_reported_and_writes_stay_in_bounds(tpc):
     assert err(dx, rdx) <= FP32_TOL
     assert err(dw, rdw[perm]) <= FP32_TOL
     assert err(dsh, rdsh[perm]) <= FP32_TOL
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_backward_empty_graph_zeroes_dx(tpc, path):
+    """No edges: dx is all zeros (every source row written), dw and dsh are empty."""
+    prob = make_problem(*SHAPES[0], n_src=10, n_dst=7, E=0, seed=1)
+    g_np = np.random.default_rng(2).standard_normal((7, prob["plan"].dim_out))
+    desc = tpc.tp_desc_create(*prob["irreps"])
+    g = gpu_sorted_inputs(tpc, prob)
+    sp, srp, _ = tpc.tp_csr_build(g["src"], prob["n_src"])
+    dx = torch.full((10, desc.dim_x), 5.0, device="cuda")
+    with tuning(tpc, **PATHS[path]):
+        _, dw, dsh = tpc.tp_conv_backward(desc, dev_tensor(g_np), g["x"], g["sh"], g["w"], g["src"], g["dst"],
+                                          g["row_ptr"], sp, srp, dx=dx)
+        torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+    assert not dx.any() and dw.numel() == 0 and dsh.numel() == 0

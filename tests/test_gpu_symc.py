@@ -74,3 +74,14 @@ def test_symmetric_contraction_bad_element(tpc, path):
     keep = np.arange(50) != 7
     ref = symc.symmetric_contraction(plan, x[keep].astype(np.float64), w.astype(np.float64), el[keep])
     assert err(out[torch.as_tensor(keep, device="cuda")], ref) <= FP32_TOL
+
+
+def test_symmetric_contraction_no_nodes(tpc):
+    s = tpc.tp_symc_create("32x0e+32x1o", "32x0e", 3)
+    x = torch.zeros((0, s.dim_in), device="cuda")
+    w = torch.zeros((2, s.n_weights, s.mul), device="cuda")
+    el = torch.zeros((0,), dtype=torch.int32, device="cuda")
+    out = tpc.tp_symmetric_contraction(s, x, w, el)
+    torch.cuda.synchronize()
+    assert out.shape == (0, s.dim_out)
+    assert tpc.tp_device_status(reset=True) == 0
