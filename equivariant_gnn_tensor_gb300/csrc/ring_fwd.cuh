@@ -515,6 +515,7 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     int n_done = 0, s_done = 0;
     uint32_t ph_done = 0;
     bool failed = false;
+    int failed_j = 0;  // the piece whose wait gave up
     for (int j = 0; j < np_w && !failed; ++j) {
         const int p = gw + j * nW;
         const int e_lo = piece_lo(p), e_hi = piece_lo(p + 1);
@@ -573,16 +574,8 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         while (e < e_hi) {
             const int s = s_done;
             if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph_done, prm.wait_ns))) {
-                if (lane == 0) {
-                    set_status(prm.status, TP_DEV_ERR_TIMEOUT);
-                    // this piece's partial rows and those of the pieces never
-                    // reached are not written: the merge must skip them
-                    for (int j2 = j; j2 < np_w; ++j2) {
-                        prm.carry_dst[2 * (gw + j2 * nW)] = -1;
-                        prm.carry_dst[2 * (gw + j2 * nW) + 1] = -1;
-                    }
-                }
-                failed = true;
+                failed = true;  // reported, and its pieces marked, after the loop
+                failed_j = j;
                 break;
             }
             const int n = min(eps, e_hi - e);
@@ -740,6 +733,15 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         }
     }
     if (failed) {
+        if (lane == 0) {
+            set_status(prm.status, TP_DEV_ERR_TIMEOUT);
+            // the partial rows of the piece that failed and of the pieces never
+            // reached are not written: the merge must skip them
+            for (int j2 = failed_j; j2 < np_w; ++j2) {
+                prm.carry_dst[2 * (gw + j2 * nW)] = -1;
+                prm.carry_dst[2 * (gw + j2 * nW) + 1] = -1;
+            }
+        }
         // let the copies still in flight land (full time limit) before the
         // shared memory is released
         for (int k = n_done; k < n_issued; ++k) {
