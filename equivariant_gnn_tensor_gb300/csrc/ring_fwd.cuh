@@ -88,6 +88,16 @@ __global__ void carry_fixup_kernel(const float *__restrict__ carry, const int32_
 // Width of the radial network's hidden layer (Linear(1, 16) -> SiLU -> Linear(16, P*mul)).
 constexpr int kMlpHidden = 16;
 
+// The radial network with edge pairs (one channel per lane, at most
+// kMlpMaxPaths paths) forms the weights in registers, two edges per packed
+// FMA: the block keeps a copy of the second layer arranged by lane,
+// [i][j][lane][4] = {w2[i][2j][c] twice, w2[i][2j+1][c] twice} (zero past the
+// last path; i = kMlpHidden holds the bias), and a chunk of at most kMlpChunk
+// edges reads that copy once and gets its weights, paired by edge, by 16
+// packed FMAs each.
+constexpr int kMlpChunk = 8, kMlpMaxPaths = 8;
+constexpr int kMlpW2sBytes = (kMlpHidden + 1) * 4 * 32 * 16;
+
 struct RingParams {
     int32_t S, eps;                      // stages per warp, edges per chunk (<= 30)
     int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0, source rows, harmonic span
@@ -97,7 +107,8 @@ struct RingParams {
     int32_t h_off;                       // warp region (VM == 2): hidden activations [eps][kMlpHidden]
     const float *mlp_w1, *mlp_b1;        // VM == 2: [H], [H]
     const float *mlp_w2, *mlp_b2;        // VM == 2: [H][P*mul] (h-major), [P*mul]
-    int32_t tab_bytes;                   // block-shared M recipe table at the start of shared memory
+    int32_t tab_bytes;                   // block-shared bytes: the M recipe table, then (VM 2, edge pairs)
+    int32_t w2s_off;                     // the second layer's copy by lane
     uint32_t ej[kMaxM];
     float ec[kMaxM][2];
     const void *x;
@@ -234,30 +245,21 @@ constexpr int entry_at(int T, int pos) {
     return -1;
 }
 
-// One program path for one edge: acc[lc-block row k] += w_T * sum_i M_T[i][k] x[la-block row i].
-// wl: this lane's channels of the edge's weight row (wlB: of the second edge,
-// edge pairs only); Mq: the edge's M (entries duplicated into pairs for channel
-// pairs, the two edges' entries interleaved for edge pairs); use_a / use_b:
-// edge pairs only, whether each edge takes part (an absent one adds zero).
-template <int LI, int LSH, int LO, int T, int CPT, bool PK, typename FT>
-__device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[rows_upto(LO)][LaneVec<CPT, PK>::NV],
-                                          const typename LaneVec<CPT, PK>::V (&xr)[rows_upto(LI)][LaneVec<CPT, PK>::NV],
-                                          const FT *wl, const FT *wlB, const float *Mq, bool use_a = true,
-                                          bool use_b = true) {
+// One program path for one edge: acc[lc-block row k] += w_T * sum_i M_T[i][k] x[la-block row i],
+// with this lane's weight values wv of the path given. Mq: the edge's M
+// (entries duplicated into pairs for channel pairs, the two edges' entries
+// interleaved for edge pairs).
+template <int LI, int LSH, int LO, int T, int CPT, bool PK>
+__device__ __forceinline__ void ring_path_w(typename LaneVec<CPT, PK>::V (&acc)[rows_upto(LO)][LaneVec<CPT, PK>::NV],
+                                            const typename LaneVec<CPT, PK>::V (&xr)[rows_upto(LI)][LaneVec<CPT, PK>::NV],
+                                            const typename LaneVec<CPT, PK>::V (&wv)[LaneVec<CPT, PK>::NV],
+                                            const float *Mq) {
     using LV = LaneVec<CPT, PK>;
-    constexpr int MUL = 32 * CPT;
     using V = typename LV::V;
     constexpr int NV = LV::NV;
     constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
     constexpr int LA = P.p[T].la, LC = P.p[T].lc;
     constexpr int NA = 2 * LA + 1, NC = 2 * LC + 1, NZ = P.nz[T], MO = P.moff[T];
-    V wv[NV];
-    if constexpr (LV::kEdgePair) {
-        const float a = to_float(wl[T * MUL]), b = to_float(wlB[T * MUL]);
-        wv[0] = pack2(use_a ? a : 0.f, use_b ? b : 0.f);
-    } else {
-        load_lane<CPT, PK>(wl + T * MUL, wv);
-    }
     // M entries of this path: 4 per 16-byte load (singles) or 2 (pairs)
     constexpr int PER = LV::kPair ? 2 : 4;
     constexpr int NL = (NZ + PER - 1) / PER;
@@ -317,6 +319,26 @@ __device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[ro
     }
 }
 
+// The same with the weights read from shared memory. wl: this lane's channels
+// of the edge's weight row (wlB: of the second edge, edge pairs only); use_a /
+// use_b: edge pairs only, whether each edge takes part (an absent one adds zero).
+template <int LI, int LSH, int LO, int T, int CPT, bool PK, typename FT>
+__device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[rows_upto(LO)][LaneVec<CPT, PK>::NV],
+                                          const typename LaneVec<CPT, PK>::V (&xr)[rows_upto(LI)][LaneVec<CPT, PK>::NV],
+                                          const FT *wl, const FT *wlB, const float *Mq, bool use_a = true,
+                                          bool use_b = true) {
+    using LV = LaneVec<CPT, PK>;
+    constexpr int MUL = 32 * CPT;
+    typename LV::V wv[LV::NV];
+    if constexpr (LV::kEdgePair) {
+        const float a = to_float(wl[T * MUL]), b = to_float(wlB[T * MUL]);
+        wv[0] = pack2(use_a ? a : 0.f, use_b ? b : 0.f);
+    } else {
+        load_lane<CPT, PK>(wl + T * MUL, wv);
+    }
+    ring_path_w<LI, LSH, LO, T, CPT, PK>(acc, xr, wv, Mq);
+}
+
 template <int CPT, bool PK>
 __device__ __forceinline__ void store_lane(float *p, const typename LaneVec<CPT, PK>::V (&v)[LaneVec<CPT, PK>::NV]) {
     if constexpr (LaneVec<CPT, PK>::kEdgePair) *p = lo_f(v[0]) + hi_f(v[0]);
@@ -353,6 +375,17 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     for (int r = threadIdx.x; r < P.R; r += blockDim.x)
         tab[r] = make_int4((int)(prm.ej[r] & 0xffffu) * 4, (int)(prm.ej[r] >> 16) * 4, __float_as_int(prm.ec[r][0]),
                            __float_as_int(prm.ec[r][1]));
+    // radial network with edge pairs: weights formed in registers from a block copy of the second layer
+    constexpr bool kMlpReg = VM == 2 && LV::kEdgePair && P.n <= kMlpMaxPaths;
+    if constexpr (kMlpReg) {
+        float *w2s = reinterpret_cast<float *>(smem + prm.w2s_off);
+        for (int t = threadIdx.x; t < (kMlpHidden + 1) * 512; t += blockDim.x) {
+            const int i = t >> 9, p = 2 * ((t >> 7) & 3) + ((t >> 1) & 1), c = (t >> 2) & 31;
+            float v = 0.f;
+            if (p < P.n) v = i < kMlpHidden ? prm.mlp_w2[i * WNUM + p * MUL + c] : prm.mlp_b2[p * MUL + c];
+            w2s[t] = v;
+        }
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int gw = blockIdx.x * (blockDim.x >> 5) + wib;
@@ -580,7 +613,35 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             }
             const int n = min(eps, e_hi - e);
             const unsigned char *sb = base + s * prm.stage_bytes;
-            if constexpr (VM == 2) {
+            if constexpr (kMlpReg) {
+                // harmonics of the chunk's edge vectors and their lengths (one
+                // edge per lane), then the hidden activations h[i][q], q < kMlpChunk
+                // (zero-length past n), each lane one q and four i
+                const float *vq = reinterpret_cast<const float *>(sb + prm.sh_off + (e * HR & 3) * 4);
+                float *Y = reinterpret_cast<float *>(base + prm.y_off);
+                float *hq = reinterpret_cast<float *>(base + prm.h_off);
+                float *rq = hq + kMlpChunk * kMlpHidden;
+                if (lane < kMlpChunk) {
+                    float r = 0.f;
+                    if (lane < n) {
+                        const float vx = vq[3 * lane], vy = vq[3 * lane + 1], vz = vq[3 * lane + 2];
+                        float yv[16];
+                        real_sh_upto<LSH>(vx, vy, vz, prm.vec_mode == 1, yv);
+#pragma unroll
+                        for (int j = 0; j < SHN; ++j) Y[lane * SHN + j] = yv[j];
+                        r = sqrtf(vx * vx + vy * vy + vz * vz);
+                    }
+                    rq[lane] = r;
+                }
+                __syncwarp();
+                const float r = rq[lane & (kMlpChunk - 1)];
+#pragma unroll
+                for (int k = 0; k < kMlpHidden * kMlpChunk / 32; ++k) {
+                    const int i = (lane >> 3) + 4 * k;
+                    const float z = fmaf(__ldg(prm.mlp_w1 + i), r, __ldg(prm.mlp_b1 + i));
+                    hq[i * kMlpChunk + (lane & (kMlpChunk - 1))] = __fdividef(z, 1.f + __expf(-z));
+                }
+            } else if constexpr (VM == 2) {
                 // weight rows of the chunk from the radial network of the edge length:
                 // h[q][i] = silu(w1[i] |v_q| + b1[i]), w[q][j] = b2[j] + sum_i w2[i][j] h[q][i]
                 const float *vq = reinterpret_cast<const float *>(sb + prm.sh_off + (e * HR & 3) * 4);
@@ -619,7 +680,9 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             // M of the chunk's edges (lane-parallel over entries)
             {
                 const unsigned char *shq = sb + prm.sh_off + (HR % 4 != 0 ? (e * HR & 3) * 4 : 0);
-                if constexpr (VEC) {
+                if constexpr (kMlpReg) {
+                    shq = reinterpret_cast<const unsigned char *>(base + prm.y_off);  // evaluated above
+                } else if constexpr (VEC) {
                     // harmonics of the chunk's edge vectors, one edge per lane
                     float *Y = reinterpret_cast<float *>(base + prm.y_off);
                     if (lane < n) {
@@ -654,7 +717,84 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             __syncwarp();
             const FT *wl = reinterpret_cast<const FT *>(sb) + ch0;
             const FT *xl = reinterpret_cast<const FT *>(sb + prm.f_off) + ch0;
-            if constexpr (LV::kEdgePair) {
+            if constexpr (kMlpReg) {
+                // this lane's weights of every edge of the chunk and path, paired
+                // by edge: wp[j][t] = (w[2j][t], w[2j+1][t]) with
+                // w[q][t] = b2[t][c] + sum_i w2[i][t][c] h[i][q], the sum in order of i
+                constexpr int NJ = (P.n + 1) / 2;
+                const ulonglong2 *w2v = reinterpret_cast<const ulonglong2 *>(smem + prm.w2s_off) + lane;
+                const ulonglong2 *h2 = reinterpret_cast<const ulonglong2 *>(base + prm.h_off);
+                f32x2 wp[kMlpChunk / 2][P.n];
+                {
+                    f32x2 bb[2 * NJ];
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) {
+                        const ulonglong2 u = w2v[(kMlpHidden * 4 + jj) * 32];
+                        bb[2 * jj] = u.x;
+                        bb[2 * jj + 1] = u.y;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kMlpChunk / 2; ++j)
+#pragma unroll
+                        for (int t = 0; t < P.n; ++t) wp[j][t] = bb[t];
+                }
+#pragma unroll
+                for (int i = 0; i < kMlpHidden; ++i) {
+                    f32x2 ww[2 * NJ];
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) {
+                        const ulonglong2 u = w2v[(i * 4 + jj) * 32];
+                        ww[2 * jj] = u.x;
+                        ww[2 * jj + 1] = u.y;
+                    }
+                    const ulonglong2 ha = h2[2 * i], hb = h2[2 * i + 1];
+                    const f32x2 hp[4] = {ha.x, ha.y, hb.x, hb.y};
+#pragma unroll
+                    for (int j = 0; j < kMlpChunk / 2; ++j)
+#pragma unroll
+                        for (int t = 0; t < P.n; ++t) vfma(wp[j][t], ww[t], hp[j]);
+                }
+                // edges (q, q+1) of an aligned pair together when they share the
+                // destination, else one at a time with the other half zeroed
+                static_for<kMlpChunk / 2>([&](auto jc) {
+                    constexpr int j = decltype(jc)::value, q = 2 * j;
+                    if (q < n) {
+                        const float *Mq = Mw + j * MS;
+                        const FT *xa = xl + q * DX;
+                        const bool has_b = q + 1 < n;
+                        const FT *xb = has_b ? xa + DX : xa;
+                        bool pa = true, pb = has_b;  // edges of the pair still to add
+                        while (pa || pb) {
+                            while (e >= seg_end && cur_d < d_end) {
+                                store_row(cur_d);
+                                ++cur_d;
+                                enter(cur_d);
+                            }
+                            const bool ua = pa, ub = pb && (!pa || e + 1 < seg_end);
+                            V xr[RI][1], wv[P.n][1];
+#pragma unroll
+                            for (int r = 0; r < RI; ++r) xr[r][0] = pack2(to_float(xa[r * MUL]), to_float(xb[r * MUL]));
+#pragma unroll
+                            for (int t = 0; t < P.n; ++t) wv[t][0] = wp[j][t];
+                            if (!(ua && ub)) {  // one edge of the pair: the other half adds zero
+#pragma unroll
+                                for (int r = 0; r < RI; ++r)
+                                    xr[r][0] = pack2(ua ? lo_f(xr[r][0]) : 0.f, ub ? hi_f(xr[r][0]) : 0.f);
+#pragma unroll
+                                for (int t = 0; t < P.n; ++t)
+                                    wv[t][0] = pack2(ua ? lo_f(wv[t][0]) : 0.f, ub ? hi_f(wv[t][0]) : 0.f);
+                            }
+                            static_for<P.n>([&](auto tc) {
+                                constexpr int T = decltype(tc)::value;
+                                ring_path_w<LI, LSH, LO, T, CPT, PK>(acc, xr, wv[T], Mq);
+                            });
+                            e += (int)ua + (int)ub;
+                            pa = false;
+                            pb = pb && !ub;
+                        }
+                    }
+                });
+            } else if constexpr (LV::kEdgePair) {
                 // edges (q, q+1) of an aligned pair together when they share the
                 // destination, else one at a time with the other half zeroed
                 for (int q = 0; q < n; q += 2) {

@@ -48,12 +48,20 @@ static size_t carry_bytes(int pieces, int dim_out) {
 
 // The part of a ring launch that does not depend on the edge count: kernel,
 // shared-memory layout, M recipe, warps per block and blocks per SM.
+struct RingKernel {
+    const void *fn = nullptr;
+    RingParams geo{};  // layout fields and M recipe only
+    int wpb = 0, smem = 0, occ = 0;
+};
 struct RingLaunch {
     const void *fn = nullptr;
     const void *fn_vec = nullptr;  // the same kernel taking edge vectors
-    const void *fn_mlp = nullptr;  // ... and computing the weight rows (float32 only; else null)
     RingParams geo{};  // layout fields and M recipe only
     int wpb = 0, smem = 0, occ = 0, rounds = 1;
+    // the kernel computing the weight rows by the radial network (float32
+    // only; fn null when there is none): the layout above, or with edge pairs
+    // its own (no weight rows in the ring, the second layer in shared memory)
+    RingKernel mlp;
 };
 
 // One warp covers all channels, CPT = mul/32 in {1,2,4} channels per lane,
@@ -84,7 +92,7 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
         if (TP.wofs[t] != t * mul) return false;
     rl.fn = dtype == TP_F32 ? ring_kernel_f32(TP.shape, cpt, pk) : ring_kernel_bf16(TP.shape, cpt, pk);
     rl.fn_vec = dtype == TP_F32 ? ring_kernel_vec_f32(TP.shape, cpt, pk) : ring_kernel_vec_bf16(TP.shape, cpt, pk);
-    rl.fn_mlp = dtype == TP_F32 ? ring_kernel_mlp_f32(TP.shape, cpt, pk) : nullptr;
+    const void *fn_mlp = dtype == TP_F32 ? ring_kernel_mlp_f32(TP.shape, cpt, pk) : nullptr;
     if (!rl.fn || !rl.fn_vec) return false;
     const int esz = dtype == TP_F32 ? 4 : 2;
     RingParams &g = rl.geo;
@@ -124,14 +132,50 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_v, rl.fn_vec, 32 * wpb, rl.smem) != cudaSuccess || occ_v < 1)
         return false;
     if (occ_v < rl.occ) rl.occ = occ_v;
-    if (rl.fn_mlp) {
+    if (fn_mlp && cpt == 1 && pk && prog.n <= kMlpMaxPaths) {
+        // edge pairs: the ring carries source rows and edge vectors only, in
+        // chunks of up to kMlpChunk edges (the weights of one chunk are formed
+        // at once), with a third stage against the longer time per chunk
+        RingKernel &m = rl.mlp;
+        RingParams &h = m.geo;
+        h = g;
+        const int per_edge_m = f_bytes + 12;
+        int em = tu.ring_stage_bytes ? (tu.ring_stage_bytes + per_edge_m - 1) / per_edge_m : kMlpChunk;
+        em = em < 1 ? 1 : (em > kMlpChunk ? kMlpChunk : em);
+        h.S = tu.ring_stages ? tu.ring_stages : 3;
+        h.eps = em;
+        h.f_off = 0;
+        h.sh_off = em * f_bytes;
+        h.stage_bytes = round_up(h.sh_off + em * 12 + 32, 128);
+        h.m_off = h.S * h.stage_bytes;
+        h.y_off = round_up(h.m_off + em * TP.R * 8, 16);
+        h.h_off = round_up(h.y_off + em * shn * 4, 16);
+        h.bar_off = round_up(h.h_off + kMlpChunk * (kMlpHidden + 1) * 4, 16);  // h, then the edge lengths
+        h.warp_bytes = round_up(h.bar_off + h.S * 8, 128);
+        h.w2s_off = round_up(16 * TP.R, 128);
+        h.tab_bytes = h.w2s_off + kMlpW2sBytes;
+        int wm = tu.ring_warps ? tu.ring_warps : 8;
+        while (wm > 1 && h.tab_bytes + wm * h.warp_bytes > smem_optin) --wm;
+        m.wpb = wm;
+        m.smem = h.tab_bytes + wm * h.warp_bytes;
+        if (m.smem <= smem_optin &&
+            cudaFuncSetAttribute(fn_mlp, cudaFuncAttributeMaxDynamicSharedMemorySize, m.smem) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m.occ, fn_mlp, 32 * wm, m.smem) == cudaSuccess &&
+            m.occ >= 1)
+            m.fn = fn_mlp;
+    } else if (fn_mlp) {
+        // otherwise the layout of the other two, at the smallest occupancy of the three
         int occ_m = 0;
-        if (cudaFuncSetAttribute(rl.fn_mlp, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_m, rl.fn_mlp, 32 * wpb, rl.smem) != cudaSuccess ||
-            occ_m < 1)
-            rl.fn_mlp = nullptr;
-        else if (occ_m < rl.occ)
-            rl.occ = occ_m;
+        if (cudaFuncSetAttribute(fn_mlp, cudaFuncAttributeMaxDynamicSharedMemorySize, rl.smem) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_m, fn_mlp, 32 * wpb, rl.smem) == cudaSuccess &&
+            occ_m >= 1) {
+            if (occ_m < rl.occ) rl.occ = occ_m;
+            rl.mlp.fn = fn_mlp;
+            rl.mlp.geo = g;
+            rl.mlp.wpb = rl.wpb;
+            rl.mlp.smem = rl.smem;
+            rl.mlp.occ = rl.occ;
+        }
     }
     rl.rounds = tu.ring_rounds ? tu.ring_rounds : 1;
     return true;
@@ -178,13 +222,13 @@ static const RingLaunch *cached_plan(const tp_desc *d, tp_dtype dtype, int dev, 
 // edges (one or two chunks) per warp. A warp walks its chunks one ring stage
 // after another, so on a small graph spreading the edges over more warps keeps
 // every chunk in flight at once instead of paying one copy latency per chunk.
-static void ring_geometry(const RingLaunch &rl, int64_t E, int sms, int &n_warps, int &n_pieces) {
-    long long nw = (long long)sms * rl.occ * rl.wpb;
+static void ring_geometry(int occ, int wpb, int rounds, int64_t E, int sms, int &n_warps, int &n_pieces) {
+    long long nw = (long long)sms * occ * wpb;
     const long long by_edges = (E + 7) / 8;
     if (nw > by_edges) nw = by_edges;
     if (nw < 1) nw = 1;
     n_warps = (int)nw;
-    n_pieces = n_warps * rl.rounds;
+    n_pieces = n_warps * rounds;
 }
 
 // Workspace the split forward needs (0: this descriptor has no program kernel
@@ -194,9 +238,10 @@ size_t split_workspace_bytes(const tp_desc *d, tp_dtype dtype, int64_t E, int de
     if (ts.t.disable_split || E >= (int64_t)1 << 31) return 0;
     const RingLaunch *rl = cached_plan(d, dtype, dev, smem_optin, ts);
     if (!rl) return 0;
-    int nw, np;
-    ring_geometry(*rl, E, sms, nw, np);
-    return carry_bytes(np, d->tab.dim_out);
+    int nw, np, nwm = 0, npm = 0;
+    ring_geometry(rl->occ, rl->wpb, rl->rounds, E, sms, nw, np);
+    if (rl->mlp.fn) ring_geometry(rl->mlp.occ, rl->mlp.wpb, rl->rounds, E, sms, nwm, npm);
+    return carry_bytes(np > npm ? np : npm, d->tab.dim_out);
 }
 
 // Launches the ring kernel (+ partial merge). Returns cudaErrorNotSupported
@@ -216,20 +261,23 @@ cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const
     if ((al & 15u) != 0) return cudaErrorNotSupported;
     const RingLaunch *rl = cached_plan(d, dtype, dev, smem_optin, ts);
     if (!rl) return cudaErrorNotSupported;
+    if (mlp && (!rl->mlp.fn || vec_mode == 0)) return cudaErrorNotSupported;
     const Tables &T = d->tab;
+    const void *fn = mlp ? rl->mlp.fn : (vec_mode ? rl->fn_vec : rl->fn);
+    const int occ = mlp ? rl->mlp.occ : rl->occ, wpb_k = mlp ? rl->mlp.wpb : rl->wpb;
+    const int smem_k = mlp ? rl->mlp.smem : rl->smem;
     int n_warps, n_pieces;
-    ring_geometry(*rl, E, sms, n_warps, n_pieces);
+    ring_geometry(occ, wpb_k, rl->rounds, E, sms, n_warps, n_pieces);
     // a smaller caller workspace: fewer warps
     while (n_warps > 1 && carry_bytes(n_warps * rl->rounds, T.dim_out) > ws_bytes) n_warps = (n_warps + 1) / 2;
     n_pieces = n_warps * rl->rounds;
     if (carry_bytes(n_pieces, T.dim_out) > ws_bytes) return cudaErrorNotSupported;
     static_assert(sizeof(RingParams) < 32000, "kernel parameter block too large");
-    RingParams prm = rl->geo;
+    RingParams prm = mlp ? rl->mlp.geo : rl->geo;
     prm.x = x;
     prm.sh = sh;
     prm.vec_mode = vec_mode;
     if (mlp) {
-        if (!rl->fn_mlp || vec_mode == 0) return cudaErrorNotSupported;
         prm.mlp_w1 = mlp->w1;
         prm.mlp_b1 = mlp->b1;
         prm.mlp_w2 = mlp->w2;
@@ -249,10 +297,9 @@ cudaError_t split_forward(const tp_desc *d, tp_dtype dtype, const void *x, const
     prm.n_pieces = n_pieces;
     prm.E = E;
     prm.wait_ns = ts.t.wait_limit_ns > 0 ? (uint64_t)ts.t.wait_limit_ns : kWaitNs;
-    const int blocks = (n_warps + rl->wpb - 1) / rl->wpb;
+    const int blocks = (n_warps + wpb_k - 1) / wpb_k;
     void *args[] = {&prm};
-    const void *fn = mlp ? rl->fn_mlp : (vec_mode ? rl->fn_vec : rl->fn);
-    cudaError_t e = cudaLaunchKernel(fn, dim3(blocks), dim3(32 * rl->wpb), args, (size_t)rl->smem, stream);
+    cudaError_t e = cudaLaunchKernel(fn, dim3(blocks), dim3(32 * wpb_k), args, (size_t)smem_k, stream);
     if (e != cudaSuccess) return e;
     const int wpb = 8;
     carry_fixup_kernel<<<(n_pieces + wpb - 1) / wpb, 32 * wpb, 0, stream>>>(prm.carry, prm.carry_dst, n_pieces,

@@ -326,3 +326,81 @@ def test_forward_with_radial_network(tpc, irr):
     ref = tp.conv_forward(pl, rounded(prob["x"], torch.float32), prob["sh"], prob["w"], prob["src"], prob["dst"],
                           prob["n_dst"])
     assert err(out, ref) <= FP32_TOL
+
+
+RADIAL_GEOMETRIES = {
+    "default": {},
+    "eps1-S2-w1": dict(ring_stage_bytes=1, ring_stages=2, ring_warps=1),
+    "eps3-S4": dict(ring_stage_bytes=1500, ring_stages=4),
+    "S8-w8": dict(ring_stages=8, ring_warps=8),
+    "rounds5": dict(ring_rounds=5),
+    "nopack": dict(ring_pack=2),
+}
+
+
+@pytest.mark.parametrize("geo", list(RADIAL_GEOMETRIES))
+@pytest.mark.parametrize("irr", [SHAPES[0], SHAPES[3]], ids=["cpt1", "lesson"])
+def test_radial_network_geometries(tpc, irr, geo):
+    """The radial-network forward with edge pairs (a chunk's weights formed in
+    registers from the block's copy of the second layer) in chunks of 1, 3 and
+    8 edges, 2 to 8 stages, 1 to 8 warps, several pieces per warp, and the
+    one-edge-at-a-time kernel (nopack), on a graph with a 1000-edge destination
+    cut across pieces, destinations of one edge between longer ones (pairs
+    split across destinations), empty destinations and a ragged tail: every
+    row against the oracle's radial network and harmonics (fp64) of the same
+    float32 inputs."""
+    from workloads import make_radial_mlp
+    rng = np.random.default_rng(77)
+    n_dst = 500
+    dst = np.concatenate([np.full(1000, 7), rng.integers(0, n_dst // 2, 5003) * 2, [n_dst - 1],
+                          np.arange(1, 60, 2)])
+    rng.shuffle(dst)
+    prob = make_problem(*irr, n_src=300, n_dst=n_dst, E=len(dst), seed=78, dst=dst)
+    pl = prob["plan"]
+    w1, b1, w2, b2 = make_radial_mlp(78, 0, 16, pl.weight_numel)
+    v32 = rounded(prob["vec"], torch.float32)
+    prob["w"] = tp.radial_mlp(v32, w1, b1, w2, b2)
+    prob["sh"] = so3.sh_concat([t.l for t in pl.irr_sh], v32)
+    desc = tpc.tp_desc_create(*irr)
+    g = gpu_sorted_inputs(tpc, prob)
+    vec = dev_tensor(prob["vec"])[g["perm"].long()].contiguous()
+    with tuning(tpc, disable_mma=1, **RADIAL_GEOMETRIES[geo]):
+        out = tpc.tp_conv_forward_mlp(desc, g["x"], vec, dev_tensor(w1), dev_tensor(b1), dev_tensor(w2),
+                                      dev_tensor(b2), g["src"], g["row_ptr"], n_dst)
+        torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+    ref = tp.conv_forward(pl, rounded(prob["x"], torch.float32), prob["sh"], prob["w"], prob["src"], prob["dst"],
+                          n_dst)
+    on = out.double().cpu().numpy()
+    for d, c in zip(*np.unique(dst, return_counts=True)):
+        assert err(on[d], ref[d]) <= deg_tol(c), d
+    empty = np.setdiff1d(np.arange(n_dst), dst)
+    assert len(empty) > 100 and not out[torch.as_tensor(empty)].any()
+
+
+def test_radial_network_out_of_range_source(tpc):
+    """An edge whose source is out of range adds nothing and sets
+    TP_DEV_ERR_INDEX; the other edges match the oracle without it."""
+    from workloads import make_radial_mlp
+    prob = make_problem(*SHAPES[0], n_src=64, n_dst=64, E=2000, seed=79)
+    pl = prob["plan"]
+    w1, b1, w2, b2 = make_radial_mlp(79, 0, 16, pl.weight_numel)
+    v32 = rounded(prob["vec"], torch.float32)
+    prob["w"] = tp.radial_mlp(v32, w1, b1, w2, b2)
+    prob["sh"] = so3.sh_concat([t.l for t in pl.irr_sh], v32)
+    desc = tpc.tp_desc_create(*SHAPES[0])
+    g = gpu_sorted_inputs(tpc, prob)
+    vec = dev_tensor(prob["vec"])[g["perm"].long()].contiguous()
+    bad = g["src"].clone()
+    bad[17] = 64
+    bad[1001] = -5
+    out = tpc.tp_conv_forward_mlp(desc, g["x"], vec, dev_tensor(w1), dev_tensor(b1), dev_tensor(w2), dev_tensor(b2),
+                                  bad, g["row_ptr"], 64)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) & tpc.TP_DEV_ERR_INDEX
+    keep = np.ones(2000, bool)
+    keep[g["perm"].cpu().numpy()[[17, 1001]]] = False
+    ref = tp.conv_forward(pl, rounded(prob["x"], torch.float32), prob["sh"][keep], prob["w"][keep],
+                          prob["src"][keep], prob["dst"][keep], 64)
+    assert err(out, ref) <= FP32_TOL
+    assert tpc.tp_device_status(reset=True) == 0

@@ -65,6 +65,47 @@ def test_fullsize_sampled_rows(tpc, name):
             assert not np.any(g)
 
 
+def test_fullsize_radial_network_sampled_rows(tpc):
+    """The very large workload through tp_conv_forward_mlp as bench.py times
+    it (harmonics and the radial network Linear(1,16)-SiLU-Linear(16,224) of
+    the float32 edge vectors evaluated in the kernel, the benchmark's
+    workspace): sampled rows against the fp64 C oracle, with the oracle's
+    radial network and harmonics of the same float32 vectors."""
+    import bench
+    from workloads import make_radial_mlp
+    dev = torch.device("cuda:0")
+    wl, desc, inp, n, E, host = bench.build_inputs("xlarge", 0, tpc, torch, dev)
+    x, _, src, dst, vec, _ = host
+    del inp["w"], inp["sh"]
+    mlp = make_radial_mlp(0, wl.wid, 16, desc.weight_numel)
+    ws = torch.empty(tpc.tp_conv_forward_workspace_size(desc, tpc.TP_F32, n, E), dtype=torch.uint8, device=dev)
+    out = tpc.tp_conv_forward_mlp(desc, inp["x"], inp["vec"], *(torch.as_tensor(a).to(dev) for a in mlp),
+                                  inp["src"], inp["row_ptr"], n, workspace=ws)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
+
+    plan = tp.Plan(wl.irreps_in, wl.irreps_sh, wl.irreps_out)
+    order = np.argsort(dst, kind="stable")
+    row_ptr = np.zeros(n + 1, dtype=np.int64)
+    np.cumsum(np.bincount(dst, minlength=n), out=row_ptr[1:])
+    rows = _sample_rows(np.random.default_rng(321), row_ptr, n)
+    sel = np.concatenate([order[row_ptr[r]:row_ptr[r + 1]] for r in rows])
+    lrp = np.zeros(len(rows) + 1, dtype=np.int64)
+    np.cumsum(row_ptr[rows + 1] - row_ptr[rows], out=lrp[1:])
+    v = vec[sel].astype(np.float32).astype(np.float64)
+    ws_ref = tp.radial_mlp(v, *mlp)
+    sh = so3.sh_concat([t.l for t in plan.irr_sh], v)
+    ref = cref.conv_forward(plan, x.astype(np.float64), sh, ws_ref, src[sel], lrp, len(rows))
+    got = out[torch.as_tensor(rows, device=dev)].double().cpu().numpy()
+    deg = row_ptr[rows + 1] - row_ptr[rows]
+    assert err(got, ref) <= FP32_TOL
+    for g, r, d in zip(got, ref, deg):
+        if d:
+            assert err(g, r) <= deg_tol(int(d))
+        else:
+            assert not np.any(g)
+
+
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
 def test_backward_fwdbwd_fullsize(tpc, bf16):
     """The backward of the fwd+bwd configuration at its full size (the medium
