@@ -91,12 +91,16 @@ constexpr int kMlpHidden = 16;
 // The radial network with edge pairs (one channel per lane, at most
 // kMlpMaxPaths paths) forms the weights in registers, two edges per packed
 // FMA: the block keeps a copy of the second layer arranged by lane,
-// [i][j][lane][4] = {w2[i][2j][c] twice, w2[i][2j+1][c] twice} (zero past the
-// last path; i = kMlpHidden holds the bias), and a chunk of at most kMlpChunk
-// edges reads that copy once and gets its weights, paired by edge, by 16
-// packed FMAs each.
+// [i][half][lane][4] = w2[i][4*half .. 4*half+3][c] (zero past the last path;
+// i = kMlpHidden holds the bias), and a chunk of at most kMlpChunk edges reads
+// that copy once and gets its weights, paired by edge, by 16 packed FMAs each
+// (the value splatted into both halves in registers). kMlpSplat keeps the
+// splatted pairs in shared memory instead, [i][j][lane][4] = {w2[i][2j][c]
+// twice, w2[i][2j+1][c] twice}: no register moves, but twice the
+// shared-memory reads, which measured 5 % slower.
 constexpr int kMlpChunk = 8, kMlpMaxPaths = 8;
-constexpr int kMlpW2sBytes = (kMlpHidden + 1) * 4 * 32 * 16;
+constexpr bool kMlpSplat = false;
+constexpr int kMlpW2sBytes = (kMlpHidden + 1) * (kMlpSplat ? 4 : 2) * 32 * 16;
 
 struct RingParams {
     int32_t S, eps;                      // stages per warp, edges per chunk (<= 30)
@@ -379,8 +383,9 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     constexpr bool kMlpReg = VM == 2 && LV::kEdgePair && P.n <= kMlpMaxPaths;
     if constexpr (kMlpReg) {
         float *w2s = reinterpret_cast<float *>(smem + prm.w2s_off);
-        for (int t = threadIdx.x; t < (kMlpHidden + 1) * 512; t += blockDim.x) {
-            const int i = t >> 9, p = 2 * ((t >> 7) & 3) + ((t >> 1) & 1), c = (t >> 2) & 31;
+        for (int t = threadIdx.x; t < kMlpW2sBytes / 4; t += blockDim.x) {
+            const int i = kMlpSplat ? t >> 9 : t >> 8, c = (t >> 2) & 31;
+            const int p = kMlpSplat ? 2 * ((t >> 7) & 3) + ((t >> 1) & 1) : 4 * ((t >> 7) & 1) + (t & 3);
             float v = 0.f;
             if (p < P.n) v = i < kMlpHidden ? prm.mlp_w2[i * WNUM + p * MUL + c] : prm.mlp_b2[p * MUL + c];
             w2s[t] = v;
@@ -721,18 +726,33 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                 // this lane's weights of every edge of the chunk and path, paired
                 // by edge: wp[j][t] = (w[2j][t], w[2j+1][t]) with
                 // w[q][t] = b2[t][c] + sum_i w2[i][t][c] h[i][q], the sum in order of i
-                constexpr int NJ = (P.n + 1) / 2;
-                const ulonglong2 *w2v = reinterpret_cast<const ulonglong2 *>(smem + prm.w2s_off) + lane;
                 const ulonglong2 *h2 = reinterpret_cast<const ulonglong2 *>(base + prm.h_off);
+                // (w2[i][t][c], w2[i][t][c]) for t < P.n (i = kMlpHidden: the bias)
+                auto w2_pairs = [&](int i, f32x2 (&ww)[8]) {
+                    if constexpr (kMlpSplat) {
+                        const ulonglong2 *w2v = reinterpret_cast<const ulonglong2 *>(smem + prm.w2s_off) + lane;
+#pragma unroll
+                        for (int jj = 0; jj < (P.n + 1) / 2; ++jj) {
+                            const ulonglong2 u = w2v[(i * 4 + jj) * 32];
+                            ww[2 * jj] = u.x;
+                            ww[2 * jj + 1] = u.y;
+                        }
+                    } else {
+                        const float4 *w2v = reinterpret_cast<const float4 *>(smem + prm.w2s_off) + lane;
+#pragma unroll
+                        for (int hh = 0; hh < (P.n + 3) / 4; ++hh) {
+                            const float4 u = w2v[(i * 2 + hh) * 32];
+                            ww[4 * hh] = pack2(u.x, u.x);
+                            ww[4 * hh + 1] = pack2(u.y, u.y);
+                            ww[4 * hh + 2] = pack2(u.z, u.z);
+                            ww[4 * hh + 3] = pack2(u.w, u.w);
+                        }
+                    }
+                };
                 f32x2 wp[kMlpChunk / 2][P.n];
                 {
-                    f32x2 bb[2 * NJ];
-#pragma unroll
-                    for (int jj = 0; jj < NJ; ++jj) {
-                        const ulonglong2 u = w2v[(kMlpHidden * 4 + jj) * 32];
-                        bb[2 * jj] = u.x;
-                        bb[2 * jj + 1] = u.y;
-                    }
+                    f32x2 bb[8];
+                    w2_pairs(kMlpHidden, bb);
 #pragma unroll
                     for (int j = 0; j < kMlpChunk / 2; ++j)
 #pragma unroll
@@ -740,13 +760,8 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                 }
 #pragma unroll
                 for (int i = 0; i < kMlpHidden; ++i) {
-                    f32x2 ww[2 * NJ];
-#pragma unroll
-                    for (int jj = 0; jj < NJ; ++jj) {
-                        const ulonglong2 u = w2v[(i * 4 + jj) * 32];
-                        ww[2 * jj] = u.x;
-                        ww[2 * jj + 1] = u.y;
-                    }
+                    f32x2 ww[8];
+                    w2_pairs(i, ww);
                     const ulonglong2 ha = h2[2 * i], hb = h2[2 * i + 1];
                     const f32x2 hp[4] = {ha.x, ha.y, hb.x, hb.y};
 #pragma unroll
