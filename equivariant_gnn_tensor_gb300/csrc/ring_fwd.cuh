@@ -15,9 +15,9 @@
 // Per warp:
 //   issue:   chunks of up to `eps` consecutive edges of its pieces, in order;
 //            one bulk copy for the chunk's weight rows, one for the 16-byte
-//            aligned span around its harmonic rows, one per edge for the
-//            gathered source row x[src[e]] (each copy from its own lane, so
-//            all of them issue as one instruction). The source indices of the
+//            aligned span around its harmonic rows (each from its own lane),
+//            and the gathered source rows x[src[e]] by 16-byte cp.async, every
+//            lane a 16-byte slice of each row. The source indices of the
 //            next two chunks are loaded ahead into registers; an out-of-range
 //            source sets a status bit and its edge gets a zero row.
 //   consume: wait for the chunk's stage, build the per-edge matrices
@@ -399,8 +399,13 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     unsigned char *base = smem + prm.tab_bytes + (size_t)wib * prm.warp_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(base + prm.bar_off);
     float *Mw = reinterpret_cast<float *>(base + prm.m_off);
+    // kXAsync: source rows by 16-byte cp.async per lane (the load/store unit)
+    // instead of one bulk copy per row (measured 1-3 % faster on every program
+    // shape); the stage's barrier then also takes one arrival per lane, when
+    // that lane's copies have landed
+    constexpr bool kXAsync = true;
     if (lane == 0)
-        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], kXAsync ? 33 : 1);
     fence_barrier_init();
     if constexpr (LV::kEdgePair)  // an absent second edge reads finite (zero) M entries
         for (int i = lane; i < eps * MS; i += 32) Mw[i] = 0.f;
@@ -481,7 +486,21 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                         *reinterpret_cast<uint4 *>(sb + prm.f_off + q * FB + o) = make_uint4(0, 0, 0, 0);
         }
         const uint32_t w_tma = VM == 2 ? 0u : (uint32_t)n * WB;  // VM 2: weight rows computed, not copied
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], w_tma + (uint32_t)__popc(okmask) * FB + sh_tma);
+        const uint32_t x_tma = kXAsync ? 0u : (uint32_t)__popc(okmask) * FB;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], w_tma + x_tma + sh_tma);
+        if constexpr (kXAsync) {
+            const unsigned char *xg = reinterpret_cast<const unsigned char *>(xp);
+            for (int q = 0; q < n; ++q) {  // warp-uniform: every lane takes part in every shuffle
+                const int sq = __shfl_sync(0xffffffffu, srcA, q);
+                if ((okmask >> q) & 1u) {
+                    const unsigned char *g = xg + (int64_t)sq * FB;
+                    unsigned char *d = sb + prm.f_off + q * FB;
+#pragma unroll
+                    for (int o = lane * 16; o < FB; o += 512) cp_async16(d + o, g + o);
+                }
+            }
+            cp_async_mbar_arrive_noinc(&full[s]);
+        }
         __syncwarp();
         // one copy per lane: lane 0 the weight rows, lane 1 the harmonic span,
         // lane 2 + q the source row of edge q
@@ -498,7 +517,7 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
         } else if (lane >= 2) {
             gsrc = xp + (int64_t)xs * DX;
             sdst = sb + prm.f_off + q * FB;
-            nbytes = (q < n && ((okmask >> q) & 1u)) ? (uint32_t)FB : 0u;
+            nbytes = (!kXAsync && q < n && ((okmask >> q) & 1u)) ? (uint32_t)FB : 0u;
             pol = pol_keep;
         }
         if (nbytes) bulk_g2s(sdst, gsrc, nbytes, &full[s], pol);
