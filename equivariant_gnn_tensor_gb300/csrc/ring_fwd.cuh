@@ -680,25 +680,42 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                 }
                 __syncwarp();
                 float *wrows = reinterpret_cast<float *>(const_cast<unsigned char *>(sb));
-                for (int j = lane; j < WNUM; j += 32) {
-                    float w2c[H];
+                // U columns per lane at a time: U independent 16-FMA chains (and
+                // their 16*U loads in flight) instead of one, where the register
+                // budget allows (one block per SM); each column's sum keeps its order
+                constexpr int U = MINB == 1 ? 8 : 1;
+                auto columns = [&](int j, auto uc) {
+                    constexpr int NU = decltype(uc)::value;
+                    float w2c[NU][H], bj[NU];
 #pragma unroll
-                    for (int i = 0; i < H; ++i) w2c[i] = __ldg(prm.mlp_w2 + i * WNUM + j);
-                    const float bj = __ldg(prm.mlp_b2 + j);
+                    for (int u = 0; u < NU; ++u) {
+#pragma unroll
+                        for (int i = 0; i < H; ++i) w2c[u][i] = __ldg(prm.mlp_w2 + i * WNUM + j + 32 * u);
+                        bj[u] = __ldg(prm.mlp_b2 + j + 32 * u);
+                    }
                     for (int q = 0; q < n; ++q) {
                         const float4 *h4 = reinterpret_cast<const float4 *>(hq + q * H);
-                        float a = bj;
+                        float a[NU];
+#pragma unroll
+                        for (int u = 0; u < NU; ++u) a[u] = bj[u];
 #pragma unroll
                         for (int i4 = 0; i4 < H / 4; ++i4) {
                             const float4 hv = h4[i4];
-                            a = fmaf(w2c[4 * i4], hv.x, a);
-                            a = fmaf(w2c[4 * i4 + 1], hv.y, a);
-                            a = fmaf(w2c[4 * i4 + 2], hv.z, a);
-                            a = fmaf(w2c[4 * i4 + 3], hv.w, a);
+#pragma unroll
+                            for (int u = 0; u < NU; ++u) {
+                                a[u] = fmaf(w2c[u][4 * i4], hv.x, a[u]);
+                                a[u] = fmaf(w2c[u][4 * i4 + 1], hv.y, a[u]);
+                                a[u] = fmaf(w2c[u][4 * i4 + 2], hv.z, a[u]);
+                                a[u] = fmaf(w2c[u][4 * i4 + 3], hv.w, a[u]);
+                            }
                         }
-                        wrows[q * WNUM + j] = a;
+#pragma unroll
+                        for (int u = 0; u < NU; ++u) wrows[q * WNUM + j + 32 * u] = a[u];
                     }
-                }
+                };
+                int j = lane;
+                for (; j + 32 * (U - 1) < WNUM; j += 32 * U) columns(j, std::integral_constant<int, U>{});
+                for (; j < WNUM; j += 32) columns(j, std::integral_constant<int, 1>{});
                 __syncwarp();
             }
             // M of the chunk's edges (lane-parallel over entries)
