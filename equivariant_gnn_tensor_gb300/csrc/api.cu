@@ -263,7 +263,7 @@ tp_status forward_core(const tp_desc *desc, const FwdArgs &a, cudaStream_t strea
                                           (a.vec_mode ? !aligned16(a.sh) : !aligned4(a.sh)))))
         return TP_ERR_ALIGN;
     if (a.mlp && a.E > 0 &&
-        (!aligned4(a.mlp->w1) || !aligned4(a.mlp->b1) || !aligned4(a.mlp->w2) || !aligned4(a.mlp->b2)))
+        (!aligned4(a.mlp->w1) || !aligned4(a.mlp->b1) || !aligned16(a.mlp->w2) || !aligned16(a.mlp->b2)))
         return TP_ERR_ALIGN;
     if (a.ws && (reinterpret_cast<uintptr_t>(a.ws) & 255u)) return TP_ERR_ALIGN;
     DevInfo dev;

@@ -343,6 +343,24 @@ __device__ __forceinline__ void ring_path(typename LaneVec<CPT, PK>::V (&acc)[ro
     ring_path_w<LI, LSH, LO, T, CPT, PK>(acc, xr, wv, Mq);
 }
 
+// CPT consecutive floats of read-only global memory (4*CPT-byte aligned).
+template <int CPT>
+__device__ __forceinline__ void ldg_lane(const float *p, float (&v)[CPT]) {
+    if constexpr (CPT == 4) {
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(p));
+        v[0] = t.x;
+        v[1] = t.y;
+        v[2] = t.z;
+        v[3] = t.w;
+    } else if constexpr (CPT == 2) {
+        const float2 t = __ldg(reinterpret_cast<const float2 *>(p));
+        v[0] = t.x;
+        v[1] = t.y;
+    } else {
+        v[0] = __ldg(p);
+    }
+}
+
 template <int CPT, bool PK>
 __device__ __forceinline__ void store_lane(float *p, const typename LaneVec<CPT, PK>::V (&v)[LaneVec<CPT, PK>::NV]) {
     if constexpr (LaneVec<CPT, PK>::kEdgePair) *p = lo_f(v[0]) + hi_f(v[0]);
@@ -381,6 +399,9 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                            __float_as_int(prm.ec[r][1]));
     // radial network with edge pairs: weights formed in registers from a block copy of the second layer
     constexpr bool kMlpReg = VM == 2 && LV::kEdgePair && P.n <= kMlpMaxPaths;
+    // radial network with plain lanes: each path's weights formed in registers
+    // just before the path, from 16-byte loads of the lane's channels of w2, b2
+    constexpr bool kMlpCols = VM == 2 && !LV::kPair;
     if constexpr (kMlpReg) {
         float *w2s = reinterpret_cast<float *>(smem + prm.w2s_off);
         for (int t = threadIdx.x; t < kMlpW2sBytes / 4; t += blockDim.x) {
@@ -679,6 +700,10 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                     hq[q * H + i] = z / (1.f + expf(-z));
                 }
                 __syncwarp();
+            }
+            if constexpr (VM == 2 && !kMlpReg && !kMlpCols) {
+                constexpr int H = kMlpHidden;
+                const float *hq = reinterpret_cast<const float *>(base + prm.h_off);
                 float *wrows = reinterpret_cast<float *>(const_cast<unsigned char *>(sb));
                 // U columns per lane at a time: U independent 16-FMA chains (and
                 // their 16*U loads in flight) instead of one, where the register
@@ -899,11 +924,38 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                     V xr[RI][NV];
 #pragma unroll
                     for (int r = 0; r < RI; ++r) load_lane<CPT, PK>(xq + r * MUL, xr[r]);
-                    const FT *wq = wl + q * (WB / (int)sizeof(FT));
                     const float *Mq = Mw + q * MS;
-                    static_for<P.n>([&](auto tc) {
-                        ring_path<LI, LSH, LO, decltype(tc)::value, CPT, PK, FT>(acc, xr, wq, wq, Mq);
-                    });
+                    if constexpr (kMlpCols) {
+                        // w[p][c] = b2[p][c] + sum_i w2[i][p][c] h[i], the sum in order of i
+                        float hv[kMlpHidden];
+                        const float4 *h4 = reinterpret_cast<const float4 *>(base + prm.h_off) + q * (kMlpHidden / 4);
+#pragma unroll
+                        for (int i4 = 0; i4 < kMlpHidden / 4; ++i4) {
+                            const float4 t = h4[i4];
+                            hv[4 * i4] = t.x;
+                            hv[4 * i4 + 1] = t.y;
+                            hv[4 * i4 + 2] = t.z;
+                            hv[4 * i4 + 3] = t.w;
+                        }
+                        static_for<P.n>([&](auto tc) {
+                            constexpr int T = decltype(tc)::value;
+                            V wv[NV];
+                            ldg_lane<CPT>(prm.mlp_b2 + T * MUL + ch0, wv);
+#pragma unroll
+                            for (int i = 0; i < kMlpHidden; ++i) {
+                                V w[NV];
+                                ldg_lane<CPT>(prm.mlp_w2 + i * WNUM + T * MUL + ch0, w);
+#pragma unroll
+                                for (int c = 0; c < NV; ++c) wv[c] = fmaf(w[c], hv[i], wv[c]);
+                            }
+                            ring_path_w<LI, LSH, LO, T, CPT, PK>(acc, xr, wv, Mq);
+                        });
+                    } else {
+                        const FT *wq = wl + q * (WB / (int)sizeof(FT));
+                        static_for<P.n>([&](auto tc) {
+                            ring_path<LI, LSH, LO, decltype(tc)::value, CPT, PK, FT>(acc, xr, wq, wq, Mq);
+                        });
+                    }
                 }
             }
             // this warp's reads of the stage come before the bulk copies that refill it

@@ -132,28 +132,29 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_v, rl.fn_vec, 32 * wpb, rl.smem) != cudaSuccess || occ_v < 1)
         return false;
     if (occ_v < rl.occ) rl.occ = occ_v;
-    if (fn_mlp && cpt == 1 && pk && prog.n <= kMlpMaxPaths) {
-        // edge pairs: the ring carries source rows and edge vectors only, in
-        // chunks of up to kMlpChunk edges (the weights of one chunk are formed
-        // at once), with a third stage against the longer time per chunk
+    // a radial-network kernel with a layout of its own: the ring carries the
+    // source rows and edge vectors only; eps from the stage target (or the
+    // given default), at most eps_max
+    auto own_layout = [&](int eps_def, int eps_max, int s_def, int m_bytes_per_edge, int h_fixed, int h_per_edge,
+                          int blk_extra) {
         RingKernel &m = rl.mlp;
         RingParams &h = m.geo;
         h = g;
         const int per_edge_m = f_bytes + 12;
-        int em = tu.ring_stage_bytes ? (tu.ring_stage_bytes + per_edge_m - 1) / per_edge_m : kMlpChunk;
-        em = em < 1 ? 1 : (em > kMlpChunk ? kMlpChunk : em);
-        h.S = tu.ring_stages ? tu.ring_stages : 3;
+        int em = tu.ring_stage_bytes ? (tu.ring_stage_bytes + per_edge_m - 1) / per_edge_m : eps_def;
+        em = em < 1 ? 1 : (em > eps_max ? eps_max : em);
+        h.S = tu.ring_stages ? tu.ring_stages : s_def;
         h.eps = em;
         h.f_off = 0;
         h.sh_off = em * f_bytes;
         h.stage_bytes = round_up(h.sh_off + em * 12 + 32, 128);
         h.m_off = h.S * h.stage_bytes;
-        h.y_off = round_up(h.m_off + em * TP.R * 8, 16);
+        h.y_off = round_up(h.m_off + em * m_bytes_per_edge, 16);
         h.h_off = round_up(h.y_off + em * shn * 4, 16);
-        h.bar_off = round_up(h.h_off + kMlpChunk * (kMlpHidden + 1) * 4, 16);  // h, then the edge lengths
+        h.bar_off = round_up(h.h_off + h_fixed + em * h_per_edge, 16);
         h.warp_bytes = round_up(h.bar_off + h.S * 8, 128);
         h.w2s_off = round_up(16 * TP.R, 128);
-        h.tab_bytes = h.w2s_off + kMlpW2sBytes;
+        h.tab_bytes = h.w2s_off + blk_extra;
         int wm = tu.ring_warps ? tu.ring_warps : 8;
         while (wm > 1 && h.tab_bytes + wm * h.warp_bytes > smem_optin) --wm;
         m.wpb = wm;
@@ -163,6 +164,19 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m.occ, fn_mlp, 32 * wm, m.smem) == cudaSuccess &&
             m.occ >= 1)
             m.fn = fn_mlp;
+    };
+    if (fn_mlp && cpt == 1 && pk && prog.n <= kMlpMaxPaths) {
+        // edge pairs: chunks of up to kMlpChunk edges (the weights of one chunk
+        // are formed at once), a third stage against the longer time per
+        // chunk, the second layer's copy block-shared; h then the edge lengths
+        own_layout(kMlpChunk, kMlpChunk, 3, TP.R * 8, kMlpChunk * (kMlpHidden + 1) * 4, 0, kMlpW2sBytes);
+    } else if (fn_mlp && !pk) {
+        // plain lanes: each path's weights formed right before the path; about
+        // 13 KB chunks (3 edges for mul 128, 7 warps per block fit: measured
+        // 591 us against 610 / 663 / 683 us for 1 / 2 / 4 edges and 635 us for
+        // a third stage); h per edge
+        const int eps_def = (13000 + f_bytes + 12 - 1) / (f_bytes + 12);
+        own_layout(eps_def < 1 ? 1 : eps_def, 30, 2, TP.R * 4, 0, kMlpHidden * 4, 0);
     } else if (fn_mlp) {
         // otherwise the layout of the other two, at the smallest occupancy of the three
         int occ_m = 0;

@@ -255,7 +255,9 @@ TPCONV_API tp_status tp_conv_forward_vec(const tp_desc *desc, tp_dtype dtype, co
  *   w[j] = b2[j] + sum_i w2[i * weight_numel + j] * h[i],             j < weight_numel
  * All pointers are device float32: w1[hidden], b1[hidden], w2[hidden][weight_numel]
  * (hidden-major, i.e. the transpose of a torch Linear(hidden, weight_numel)
- * weight), b2[weight_numel]. hidden must be 16. */
+ * weight), b2[weight_numel]. hidden must be 16. w1 and b1 4-byte aligned, w2
+ * and b2 16-byte aligned (the kernels read w2 and b2 in 16-byte pieces);
+ * TP_ERR_ALIGN otherwise. */
 typedef struct {
     const float *w1, *b1;
     const float *w2, *b2;
