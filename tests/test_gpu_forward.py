@@ -404,3 +404,25 @@ def test_radial_network_out_of_range_source(tpc):
                           prob["src"][keep], prob["dst"][keep], 64)
     assert err(out, ref) <= FP32_TOL
     assert tpc.tp_device_status(reset=True) == 0
+
+
+def test_radial_network_alignment(tpc):
+    """The radial network's w2 and b2 are read in 16-byte pieces: a w2 or b2
+    that is 4- but not 16-byte aligned is refused with TP_ERR_ALIGN before
+    anything is launched, and the aligned call succeeds."""
+    from workloads import make_radial_mlp
+    prob = make_problem(*SHAPES[1], n_src=64, n_dst=64, E=500, seed=80)
+    pl = prob["plan"]
+    desc = tpc.tp_desc_create(*SHAPES[1])
+    g = gpu_sorted_inputs(tpc, prob)
+    vec = dev_tensor(prob["vec"])[g["perm"].long()].contiguous()
+    w1, b1, w2, b2 = (dev_tensor(a) for a in make_radial_mlp(80, 0, 16, pl.weight_numel))
+    w2_off = torch.empty(w2.numel() + 1, device="cuda")[1:].view_as(w2).copy_(w2)
+    b2_off = torch.empty(b2.numel() + 1, device="cuda")[1:].copy_(b2)
+    for a, b in ((w2_off, b2), (w2, b2_off)):
+        with pytest.raises(tpc.TPError) as ei:
+            tpc.tp_conv_forward_mlp(desc, g["x"], vec, w1, b1, a, b, g["src"], g["row_ptr"], 64)
+        assert tpc.STATUS_NAMES[ei.value.status] == "TP_ERR_ALIGN"
+    tpc.tp_conv_forward_mlp(desc, g["x"], vec, w1, b1, w2, b2, g["src"], g["row_ptr"], 64)
+    torch.cuda.synchronize()
+    assert tpc.tp_device_status(reset=True) == 0
