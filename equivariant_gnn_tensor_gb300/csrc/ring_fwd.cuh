@@ -399,9 +399,10 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                            __float_as_int(prm.ec[r][1]));
     // radial network with edge pairs: weights formed in registers from a block copy of the second layer
     constexpr bool kMlpReg = VM == 2 && LV::kEdgePair && P.n <= kMlpMaxPaths;
-    // radial network with plain lanes: each path's weights formed in registers
-    // just before the path, from 16-byte loads of the lane's channels of w2, b2
-    constexpr bool kMlpCols = VM == 2 && !LV::kPair;
+    // radial network with plain lanes or channel pairs: each path's weights
+    // formed in registers just before the path, from 16-byte loads of the
+    // lane's channels of w2 and b2
+    constexpr bool kMlpCols = VM == 2 && !LV::kEdgePair;
     if constexpr (kMlpReg) {
         float *w2s = reinterpret_cast<float *>(smem + prm.w2s_off);
         for (int t = threadIdx.x; t < kMlpW2sBytes / 4; t += blockDim.x) {
@@ -939,14 +940,20 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
                         }
                         static_for<P.n>([&](auto tc) {
                             constexpr int T = decltype(tc)::value;
-                            V wv[NV];
-                            ldg_lane<CPT>(prm.mlp_b2 + T * MUL + ch0, wv);
+                            float ws[CPT];
+                            ldg_lane<CPT>(prm.mlp_b2 + T * MUL + ch0, ws);
 #pragma unroll
                             for (int i = 0; i < kMlpHidden; ++i) {
-                                V w[NV];
+                                float w[CPT];
                                 ldg_lane<CPT>(prm.mlp_w2 + i * WNUM + T * MUL + ch0, w);
 #pragma unroll
-                                for (int c = 0; c < NV; ++c) wv[c] = fmaf(w[c], hv[i], wv[c]);
+                                for (int c = 0; c < CPT; ++c) ws[c] = fmaf(w[c], hv[i], ws[c]);
+                            }
+                            V wv[NV];
+#pragma unroll
+                            for (int c = 0; c < NV; ++c) {
+                                if constexpr (LV::kPair) wv[c] = pack2(ws[2 * c], ws[2 * c + 1]);
+                                else wv[c] = ws[c];
                             }
                             ring_path_w<LI, LSH, LO, T, CPT, PK>(acc, xr, wv, Mq);
                         });

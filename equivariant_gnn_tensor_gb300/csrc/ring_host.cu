@@ -170,13 +170,14 @@ static bool ring_plan(const tp_desc *d, tp_dtype dtype, int smem_optin, const tp
         // are formed at once), a third stage against the longer time per
         // chunk, the second layer's copy block-shared; h then the edge lengths
         own_layout(kMlpChunk, kMlpChunk, 3, TP.R * 8, kMlpChunk * (kMlpHidden + 1) * 4, 0, kMlpW2sBytes);
-    } else if (fn_mlp && !pk) {
-        // plain lanes: each path's weights formed right before the path; about
+    } else if (fn_mlp && !(cpt == 1 && pk)) {
+        // plain lanes or channel pairs: each path's weights formed right before the path; about
         // 13 KB chunks (3 edges for mul 128, 7 warps per block fit: measured
         // 591 us against 610 / 663 / 683 us for 1 / 2 / 4 edges and 635 us for
         // a third stage); h per edge
         const int eps_def = (13000 + f_bytes + 12 - 1) / (f_bytes + 12);
-        own_layout(eps_def < 1 ? 1 : eps_def, 30, 2, TP.R * 4, 0, kMlpHidden * 4, 0);
+        // M per edge: R floats, or R pairs with channel pairs (entries duplicated)
+        own_layout(eps_def < 1 ? 1 : eps_def, 30, 2, TP.R * (pk ? 8 : 4), 0, kMlpHidden * 4, 0);
     } else if (fn_mlp) {
         // otherwise the layout of the other two, at the smallest occupancy of the three
         int occ_m = 0;
