@@ -369,6 +369,34 @@ __device__ __forceinline__ void store_lane(float *p, const typename LaneVec<CPT,
     else *reinterpret_cast<f32x2 *>(p) = v[0];
 }
 
+// Does the launch's shared-memory layout (RingParams offsets, dynamic size)
+// hold every region ring_fwd_kernel<...> writes? Kept out of line so the
+// kernel's own register allocation does not carry it.
+template <int LI, int LSH, int LO, int CPT, bool PK, typename FT, int VM>
+__device__ __noinline__ bool ring_layout_ok(const RingParams &prm, int warps_per_block) {
+    using LV = LaneVec<CPT, PK>;
+    constexpr Program P = NaturalProgram<LI, LSH, LO>::P;
+    constexpr int MUL = 32 * CPT, SHN = rows_upto(LSH);
+    constexpr int WB = P.n * MUL * (int)sizeof(FT), FB = rows_upto(LI) * MUL * (int)sizeof(FT);
+    constexpr int MS = LV::kPair ? 2 * P.R : P.R;
+    constexpr int HR = VM >= 1 ? 3 : SHN;
+    constexpr bool pair_mlp = VM == 2 && LV::kEdgePair && P.n <= kMlpMaxPaths;
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const int e = prm.eps;
+    return e >= 1 && e <= (pair_mlp ? kMlpChunk : 30) && prm.S >= 1 &&
+           ((prm.f_off | prm.sh_off | prm.stage_bytes | prm.m_off | prm.y_off | prm.h_off | prm.bar_off |
+             prm.warp_bytes | prm.tab_bytes) & 15) == 0 &&
+           prm.tab_bytes >= 16 * P.R &&
+           (!pair_mlp || (prm.w2s_off >= 16 * P.R && prm.w2s_off + kMlpW2sBytes <= prm.tab_bytes)) &&
+           prm.f_off >= (VM == 2 ? 0 : e * WB) && prm.sh_off >= prm.f_off + e * FB &&
+           prm.stage_bytes >= prm.sh_off + e * HR * 4 + (HR % 4 ? 32 : 0) && prm.m_off >= prm.S * prm.stage_bytes &&
+           prm.y_off >= prm.m_off + e * MS * 4 && (VM == 0 || prm.h_off >= prm.y_off + e * SHN * 4) &&
+           (VM != 2 || prm.bar_off >= prm.h_off + (pair_mlp ? kMlpChunk * (kMlpHidden + 1) : e * kMlpHidden) * 4) &&
+           prm.warp_bytes >= prm.bar_off + prm.S * 8 &&
+           (int64_t)prm.tab_bytes + (int64_t)warps_per_block * prm.warp_bytes <= (int64_t)dyn;
+}
+
 // CPT channels per lane (mul = 32*CPT), PK: packed pairs of channels. The
 // register cap follows from MINB (blocks of 256 threads per SM). VM (vector
 // mode) 0: `sh` holds harmonic rows; 1: `sh` holds edge vectors [E][3] and the
@@ -391,6 +419,13 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
     static_assert(WB % 16 == 0 && FB % 16 == 0, "bulk copies move 16-byte multiples");
     extern __shared__ __align__(128) unsigned char smem[];
     static_assert(MS % 4 == 0, "M rows are read with 16-byte loads");
+    // the launch's layout must hold everything this instantiation writes:
+    // checked before the first shared-memory store, a mismatch (a library
+    // bug) is reported and nothing runs
+    if (!ring_layout_ok<LI, LSH, LO, CPT, PK, FT, VM>(prm, blockDim.x >> 5)) {
+        if (threadIdx.x == 0) set_status(prm.status, TP_DEV_ERR_INTERNAL);
+        return;
+    }
     // block-shared recipe of the M entries: r -> {4*j0, 4*j1, c0, c1},
     // M[r] = c0 * sh[j0] + c1 * sh[j1]
     int4 *tab = reinterpret_cast<int4 *>(smem);
