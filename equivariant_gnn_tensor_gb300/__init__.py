@@ -288,9 +288,10 @@ def _ptr(t):
 
 
 def _dev_ptr(t, name, dtype=None, ndim=None):
-    torch = _torch()
+    """Device address of a checked tensor as an int (None for no tensor or
+    an empty one); the ctypes signatures take it as void*."""
     if t is None:
-        return _vp(0)
+        return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
@@ -299,13 +300,12 @@ def _dev_ptr(t, name, dtype=None, ndim=None):
         raise ValueError(f"{name} must be contiguous")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims")
-    return _vp(t.data_ptr()) if t.numel() > 0 else _vp(0)
+    return t.data_ptr() if t.numel() > 0 else None
 
 
 def _stream(stream):
-    torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return _vp(s.cuda_stream)
+    s = stream if stream is not None else _torch().cuda.current_stream()
+    return s.cuda_stream
 
 
 def tp_spherical_harmonics(desc: Descriptor, vec, normalize: bool = True, out=None, stream=None):
@@ -399,7 +399,7 @@ def tp_conv_forward(desc: Descriptor, x, sh, w, src, row_ptr, n_dst: int, out=No
     if isinstance(workspace, str):
         nb = tp_conv_forward_workspace_size(desc, dtype, n_dst, E)
         workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
-    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8)
     ws_n = workspace.numel() if workspace is not None else 0
     _check(_lib.tp_conv_forward(desc.handle, dtype, _dev_ptr(x, "x", None, 2), _dev_ptr(sh, "sh", torch.float32, 2),
                                 _dev_ptr(w, "w", None, 2), _dev_ptr(src, "src", torch.int32, 1),
@@ -421,7 +421,7 @@ def tp_conv_forward_vec(desc: Descriptor, x, vec, w, src, row_ptr, n_dst: int, n
     if isinstance(workspace, str):
         nb = tp_conv_forward_workspace_size(desc, dtype, n_dst, E)
         workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
-    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8)
     ws_n = workspace.numel() if workspace is not None else 0
     _check(_lib.tp_conv_forward_vec(desc.handle, dtype, _dev_ptr(x, "x", None, 2),
                                     _dev_ptr(vec, "vec", torch.float32, 2), int(bool(normalize)),
@@ -444,11 +444,11 @@ def tp_conv_forward_mlp(desc: Descriptor, x, vec, w1, b1, w2, b2, src, row_ptr, 
     if isinstance(workspace, str):
         nb = tp_conv_forward_workspace_size(desc, TP_F32, n_dst, E)
         workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
-    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8)
     ws_n = workspace.numel() if workspace is not None else 0
     f = torch.float32
-    mlp = _Mlp(_dev_ptr(w1, "w1", f, 1).value, _dev_ptr(b1, "b1", f, 1).value, _dev_ptr(w2, "w2", f, 2).value,
-               _dev_ptr(b2, "b2", f, 1).value, int(w1.shape[0]))
+    mlp = _Mlp(_dev_ptr(w1, "w1", f, 1), _dev_ptr(b1, "b1", f, 1), _dev_ptr(w2, "w2", f, 2),
+               _dev_ptr(b2, "b2", f, 1), int(w1.shape[0]))
     _check(_lib.tp_conv_forward_mlp(desc.handle, TP_F32 if x.dtype == f else TP_BF16_IN_F32_OUT,
                                     _dev_ptr(x, "x", None, 2), _dev_ptr(vec, "vec", f, 2), int(bool(normalize)),
                                     ctypes.byref(mlp), _dev_ptr(src, "src", torch.int32, 1),
@@ -476,21 +476,21 @@ def tp_conv_forward_ex(desc: Descriptor, x, src, row_ptr, n_dst: int, w=None, sh
     mlp_p = None
     if mlp is not None:
         w1, b1, w2, b2 = mlp
-        m = _Mlp(_dev_ptr(w1, "w1", f, 1).value, _dev_ptr(b1, "b1", f, 1).value, _dev_ptr(w2, "w2", f, 2).value,
-                 _dev_ptr(b2, "b2", f, 1).value, int(w1.shape[0]))
+        m = _Mlp(_dev_ptr(w1, "w1", f, 1), _dev_ptr(b1, "b1", f, 1), _dev_ptr(w2, "w2", f, 2),
+                 _dev_ptr(b2, "b2", f, 1), int(w1.shape[0]))
         keep.append(m)
         mlp_p = ctypes.addressof(m)
-    a = _FwdArgs(dtype, _dev_ptr(x, "x", None, 2).value, _dev_ptr(sh, "sh", f, 2).value,
-                 _dev_ptr(vec, "vec", f, 2).value, int(bool(normalize)), mlp_p, _dev_ptr(w, "w", None, 2).value,
-                 _dev_ptr(src, "src", None, 1).value, _dev_ptr(row_ptr, "row_ptr", None, 1).value,
+    a = _FwdArgs(dtype, _dev_ptr(x, "x", None, 2), _dev_ptr(sh, "sh", f, 2),
+                 _dev_ptr(vec, "vec", f, 2), int(bool(normalize)), mlp_p, _dev_ptr(w, "w", None, 2),
+                 _dev_ptr(src, "src", None, 1), _dev_ptr(row_ptr, "row_ptr", None, 1),
                  64 if src.dtype == torch.int64 else 32, {"sum": TP_REDUCE_SUM, "mean": TP_REDUCE_MEAN}[reduce],
-                 x.shape[0], n_dst, E, _dev_ptr(out, "out", f, 2).value, None, 0)
+                 x.shape[0], n_dst, E, _dev_ptr(out, "out", f, 2), None, 0)
     n = _sz()
     _check(_lib.tp_conv_forward_ex_workspace_size(desc.handle, ctypes.byref(a), ctypes.byref(n)),
            "tp_conv_forward_ex_workspace_size")
     if workspace is None:
         workspace = torch.empty(max(int(n.value), 1), dtype=torch.uint8, device=x.device)
-    a.workspace = _dev_ptr(workspace, "workspace", torch.uint8).value
+    a.workspace = _dev_ptr(workspace, "workspace", torch.uint8)
     a.workspace_bytes = workspace.numel()
     _check(_lib.tp_conv_forward_ex(desc.handle, ctypes.byref(a), _stream(stream)), "tp_conv_forward_ex")
     return out
@@ -536,7 +536,7 @@ def tp_conv_backward(desc: Descriptor, grad_out, x, sh, w, src, dst, row_ptr, sr
     if isinstance(workspace, str):
         nb = tp_conv_backward_workspace_size(desc, dtype, n_src, E)
         workspace = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
-    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8) if workspace is not None else _vp(0)
+    ws_ptr = _dev_ptr(workspace, "workspace", torch.uint8)
     ws_n = workspace.numel() if workspace is not None else 0
     f = torch.float32
     _check(_lib.tp_conv_backward(desc.handle, dtype, _dev_ptr(grad_out, "grad_out", f, 2), _dev_ptr(x, "x", None, 2),
