@@ -104,11 +104,12 @@ constexpr int kMlpW2sBytes = (kMlpHidden + 1) * (kMlpSplat ? 4 : 2) * 32 * 16;
 
 struct RingParams {
     int32_t S, eps;                      // stages per warp, edges per chunk (<= 30)
-    int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0, source rows, harmonic span
+    int32_t stage_bytes, f_off, sh_off;  // stage: weight rows at 0 (none in VM 2's own layouts), source rows, harmonic span
     int32_t m_off, bar_off, warp_bytes;  // warp region: stages, M, barriers
     int32_t y_off;                       // warp region: harmonics computed from edge vectors [eps][SHN]
     int32_t vec_mode;                    // kernels with VM >= 1: 1 harmonics of the unit vector, 2 raw polynomial
-    int32_t h_off;                       // warp region (VM == 2): hidden activations [eps][kMlpHidden]
+    int32_t h_off;                       // warp region (VM == 2): hidden activations, [eps][kMlpHidden]
+                                         // (edge pairs: [kMlpHidden][kMlpChunk], then kMlpChunk lengths)
     const float *mlp_w1, *mlp_b1;        // VM == 2: [H], [H]
     const float *mlp_w2, *mlp_b2;        // VM == 2: [H][P*mul] (h-major), [P*mul]
     int32_t tab_bytes;                   // block-shared bytes: the M recipe table, then (VM 2, edge pairs)
@@ -400,9 +401,11 @@ __device__ __noinline__ bool ring_layout_ok(const RingParams &prm, int warps_per
 // CPT channels per lane (mul = 32*CPT), PK: packed pairs of channels. The
 // register cap follows from MINB (blocks of 256 threads per SM). VM (vector
 // mode) 0: `sh` holds harmonic rows; 1: `sh` holds edge vectors [E][3] and the
-// harmonics are evaluated here; 2: as 1, and the weight rows are computed here
+// harmonics are evaluated here; 2: as 1, and the weights are computed here
 // too, by the radial network Linear(1,H) -> SiLU -> Linear(H,P*mul) of the edge
-// length, instead of streamed from `w`.
+// length, instead of streamed from `w`: with edge pairs a chunk's at once in
+// registers, with plain lanes or channel pairs each path's right before the
+// path, else (edge pairs of the larger programs) as weight rows in the stage.
 template <int LI, int LSH, int LO, int CPT, bool PK, int MINB, typename FT, int VM>
 __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(const __grid_constant__ RingParams prm) {
     using LV = LaneVec<CPT, PK>;
