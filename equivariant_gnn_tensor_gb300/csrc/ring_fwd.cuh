@@ -562,8 +562,8 @@ __global__ void __launch_bounds__(32 * kRingMaxWarps, MINB) ring_fwd_kernel(cons
             cp_async_mbar_arrive_noinc(&full[s]);
         }
         __syncwarp();
-        // one copy per lane: lane 0 the weight rows, lane 1 the harmonic span,
-        // lane 2 + q the source row of edge q
+        // one bulk copy per lane: lane 0 the weight rows, lane 1 the harmonic
+        // span, and (kXAsync false) lane 2 + q the source row of edge q
         const int xs = __shfl_up_sync(0xffffffffu, srcA, 2);
         const int q = lane - 2;
         const void *gsrc = wb + (int64_t)ic.e * WB;
