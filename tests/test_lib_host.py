@@ -101,6 +101,29 @@ def test_argument_errors_need_no_gpu(tpc):
     assert lib.tp_csr_build(good, 10, 0, good, good, vp(0), good, n.value, vp(0)) == 4
 
 
+def test_radial_network_argument_errors_need_no_gpu(tpc):
+    """The radial network's checks come before any CUDA call too, so bogus
+    addresses are never touched: w2 and b2 must be 16-byte aligned and w1, b1
+    4-byte aligned; only float32 inputs and 16 hidden units; no null pointer."""
+    lib = tpc._lib
+    d = tpc.tp_desc_create("32x0e+32x1o", "0e+1o+2e", "32x0e+32x1o+32x2e")
+    vp = ctypes.c_void_p
+    good = vp(0x10000)
+
+    def call(w1=0x20000, b1=0x20040, w2=0x30000, b2=0x40000, hidden=16, dtype=0):
+        m = tpc._Mlp(w1, b1, w2, b2, hidden)
+        st = lib.tp_conv_forward_mlp(d.handle, dtype, good, good, 1, ctypes.byref(m), good, good, 4, 4, 10, good,
+                                     vp(0), 0, vp(0))
+        return tpc.STATUS_NAMES[st]
+
+    assert call(w2=0x30004) == "TP_ERR_ALIGN"
+    assert call(b2=0x40008) == "TP_ERR_ALIGN"
+    assert call(w1=0x20002) == "TP_ERR_ALIGN"
+    assert call(hidden=8) == "TP_ERR_UNSUPPORTED"
+    assert call(dtype=tpc.TP_BF16_IN_F32_OUT) == "TP_ERR_UNSUPPORTED"
+    assert call(w2=0) == "TP_ERR_ARG"
+
+
 def test_tuning_hooks_validate_and_reset(tpc):
     """tp_set_tuning stores in-range settings, rejects out-of-range ones with
     TP_ERR_ARG (leaving the previous settings), and NULL restores defaults."""
